@@ -1,0 +1,41 @@
+"""fp64 CPU oracle for paged KV-cache append and paged attention.
+
+TEST INFRASTRUCTURE.  This package is the slow, plain statement of what the
+GPU path computes.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline / reference leg may import it; the library under
+``serving_slot_mapping_gb300`` never does, and it shares no code with it.
+It imports nothing but the Python standard library and numpy.
+
+What it follows:
+
+* append: the ScatterND write of new K/V rows into the per-layer page pool at
+  ``slot_mapping`` (onnxruntime/mobius PR #395 "Add paged / block-table KV
+  cache export", sections "How it works (per attention layer)" and "ONNX I/O
+  contract");
+* gather: ``Gather(pool, block_table)`` assembling a sequence's physical
+  pages contiguously (same page, same sections);
+* attention: softmax attention with causal + padding masking derived from
+  ``is_causal=1`` and ``nonpad_kv_seqlen`` (same page, "ONNX I/O contract"),
+  grouped-query heads where query head ``i`` reads KV head ``i // G``
+  (ROCm/maxtext PR #93 "[Draft] kv paged kernels", the KV-pool sharding
+  commit), and an explicit softmax scale (same page, the ``gpu_paged``
+  commit and the double-scaling fix);
+* the split-softmax merge identity used to combine partial results.
+
+Readings where the pages are silent are listed in the module docstring of
+:mod:`oracle.paged_attention`.
+
+Every function is pinned by the ``-m "not gpu"`` tests in ``tests/``
+(brute force, closed forms, a library attention routine on dense data,
+page-permutation and shared-prefix invariants); none is "parity unpinned".
+"""
+from .paged_attention import (  # noqa: F401
+    paged_kv_append,
+    gather_pages,
+    attend,
+    attend_partial,
+    merge_partials,
+    paged_attention_decode,
+    paged_attention_prefill,
+    paged_attention_decode_partial,
+)
