@@ -1,0 +1,568 @@
+"""Benchmark of the paged KV-cache hot path on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gqa_decode] [--no-extra]
+
+A step is one pass of the whole path over one batch: paged_kv_append of the
+step's new K/V rows at slot_mapping, then paged attention through
+block_table (decode: split kernel + combine kernel).  Inputs are synthetic,
+seeded, and resident in HBM; the L2 is flushed (256 MB write) between timed
+steps.  `value` is the decode KV-read throughput of the whole job: the
+algorithmic K+V bytes every rank's step must read, divided by the step time
+(max over ranks).
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from serving_slot_mapping_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-attn decode KV-read GB/s (% of HBM peak), tokens/s; prefill TFLOP/s"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# plumbing
+# ---------------------------------------------------------------------------
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_decode")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+def file_hash(*paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str):
+    """Per-launch DRAM bytes from a committed ncu capture, if the kernel source
+    is unchanged since the capture (else None)."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            table = json.load(f)
+        ent = table[kernel_key]
+        if ent["source_hash"] != file_hash(*ent["sources"]):
+            return None
+        return float(ent["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            text = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in text.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def timed_graph(graph, steps, flush, stream):
+    """Replay `graph` `steps` times, flushing L2 between replays; per-replay ms."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            graph.replay()
+            e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def capture(fn, stream, warm=3):
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def rank_plan(name: str, rank: int):
+    """The workload of one rank: same shapes, a rank-specific seed (weak scaling)."""
+    if rank == 0:
+        return wl.named_plan(name)
+    base = {"gqa_decode": lambda s: wl.gqa_decode_plan(seed=s),
+            "shared_prefix": lambda s: wl.shared_prefix_plan(seed=s),
+            "chunked_prefill": lambda s: wl.chunked_prefill_plan(seed=s),
+            "long_gqa": lambda s: wl.long_context_plan(hkv=8, seed=s),
+            "long_mqa": lambda s: wl.long_context_plan(hkv=1, seed=s)}[name]
+    return base(1000 + 97 * rank)
+
+
+class DecodeRig:
+    """Device-resident decode workload: append + decode graph, and a decode-only graph."""
+
+    def __init__(self, plan, dev):
+        from serving_slot_mapping_gb300 import capi
+        self.capi = capi
+        self.plan = plan
+        self.st = wl.materialize(plan, dev)
+        self.out = torch.empty_like(self.st.q)
+        self.ws = capi.decode_workspace(plan.batch, plan.num_q_heads, self.st.key_pool)
+        self.msl = int(plan.seq_lens.max())
+
+    def append(self):
+        st = self.st
+        self.capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping)
+
+    def decode(self):
+        st = self.st
+        self.capi.paged_attention_decode(st.key_pool, st.value_pool, st.q, st.block_table,
+                                         st.seq_lens, self.plan.scale, max_seq_len=self.msl,
+                                         out=self.out, workspace=self.ws)
+
+    def step(self):
+        self.append()
+        self.decode()
+
+
+class PrefillRig:
+    def __init__(self, plan, dev):
+        from serving_slot_mapping_gb300 import capi
+        self.capi = capi
+        self.plan = plan
+        self.st = wl.materialize(plan, dev)
+        self.out = torch.empty_like(self.st.q)
+        self.mql = int(plan.new.max())
+        self.msl = int(plan.seq_lens.max())
+
+    def append(self):
+        st = self.st
+        self.capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping)
+
+    def prefill(self):
+        st = self.st
+        self.capi.paged_attention_prefill(st.key_pool, st.value_pool, st.q, st.query_start_loc,
+                                          st.block_table, st.seq_lens, self.plan.scale,
+                                          max_q_len=self.mql, max_seq_len=self.msl, out=self.out)
+
+    def step(self):
+        self.append()
+        self.prefill()
+
+
+def e2e_decode(rig: DecodeRig, steps, flush):
+    """Same metric through the public API with host (pinned) inputs and output:
+    H2D of q, new K/V, slot_mapping, block_table, seq_lens; D2H of out."""
+    st = rig.st
+    names = ["q", "key", "value", "slot_mapping", "block_table", "seq_lens"]
+    host = {n: getattr(st, n).cpu().pin_memory() for n in names}
+    dev = {n: torch.empty_like(getattr(st, n)) for n in names}
+    out_h = torch.empty(rig.out.shape, dtype=rig.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    capi = rig.capi
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        capi.paged_kv_append(st.key_pool, st.value_pool, dev["key"], dev["value"],
+                             dev["slot_mapping"])
+        capi.paged_attention_decode(st.key_pool, st.value_pool, dev["q"], dev["block_table"],
+                                    dev["seq_lens"], rig.plan.scale, max_seq_len=rig.msl,
+                                    out=rig.out, workspace=rig.ws)
+        out_h.copy_(rig.out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        one()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    return ms, h2d, d2h
+
+
+class OracleRig:
+    """The fp64 CPU oracle (as it stands) on a bounded sample of a decode
+    workload: the first k sequences, with their own compact page pool (same
+    lengths, heads, page size and value distribution).  One step = oracle
+    append of the new rows + widening to fp64 + oracle decode."""
+
+    def __init__(self, plan, k):
+        k = min(plan.batch, k)
+        self.k = k
+        self.plan = wl.plan_from_lengths(plan.name + "_sample", plan.kind, plan.dtype,
+                                         plan.num_q_heads, plan.num_kv_heads, plan.head_dim,
+                                         plan.page_size, plan.cached[:k], plan.new[:k],
+                                         plan.seed, scale=plan.scale)
+        st = wl.materialize(self.plan, "cpu")
+        self.kb, self.vb = self._bits(st.key_pool), self._bits(st.value_pool)
+        self.kn, self.vn = self._bits(st.key), self._bits(st.value)
+        self.q = self._f64(self._bits(st.q))
+        self.full_batch = plan.batch
+        self.name = plan.name
+
+    @staticmethod
+    def _bits(t):
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
+            else t.numpy()
+
+    @staticmethod
+    def _f64(a):
+        if a.dtype == np.uint16:
+            return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return a.astype(np.float64)
+
+    def step(self):
+        import oracle
+        p = self.plan
+        k2, v2 = oracle.paged_kv_append(self.kb, self.vb, self.kn, self.vn, p.slot_mapping)
+        oracle.paged_attention_decode(self._f64(k2), self._f64(v2), self.q, p.block_table,
+                                      p.seq_lens, p.scale)
+
+    @property
+    def kv_bytes(self):
+        return wl.decode_kv_bytes(self.plan)
+
+    def describe(self, reps, el):
+        return (f"oracle append+decode of {self.k}/{self.full_batch} sequences of {self.name} "
+                f"(compact pool of {self.plan.num_pages} pages), {reps} reps in {el:.1f}s")
+
+
+def cpu_oracle_decode(plan, seconds: float, max_seqs=None):
+    """Time the oracle for about `seconds`: (GB/s of algorithmic KV read, s/step, desc)."""
+    rig = OracleRig(plan, plan.batch if max_seqs is None else max_seqs)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        rig.step()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    per = el / reps
+    return rig.kv_bytes / per / 1e9, per, rig.describe(reps, el)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_ours(args, rank, world, local):
+    from serving_slot_mapping_gb300 import build as build_mod
+    build_mod.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    plan = rank_plan(args.workload, rank)
+    rig = DecodeRig(plan, dev)
+    g_step = capture(rig.step, stream)
+    g_dec = capture(rig.decode, stream)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    times = timed_graph(g_step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    # dominant kernel alone (decode: split + combine), same flushing
+    dec_times = timed_graph(g_dec, max(50, args.steps // 2), flush, stream)
+    clocks = sampler.stop()
+
+    ms_step = max_over_ranks(statistics.mean(times), world)
+    kv_bytes = wl.decode_kv_bytes(plan)
+    total_kv = sum_over_ranks(float(kv_bytes), world)
+    value = total_kv / (ms_step * 1e-3) / 1e9
+    tokens_s = sum_over_ranks(float(plan.batch), world) / (ms_step * 1e-3)
+
+    dec_ms = statistics.mean(dec_times)
+    dec_bytes = kv_bytes + wl.decode_io_bytes(plan)
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = traffic_for(f"decode_split:{args.workload}")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "kernel": "paged_attention_decode (split + combine)",
+                "algorithmic_bytes_per_launch": dec_bytes,
+                "ms_per_launch": round(dec_ms, 5), "peak_source": peak_src}
+
+    e2e_ms, h2d, d2h = e2e_decode(rig, max(20, min(args.steps, 200)), flush)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e = {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_ms, 5)}
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        extra = run_extra(dev, flush, stream, hbm, bf16, bf16_sus)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        gbs, per, desc = cpu_oracle_decode(plan, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": desc, "s_per_step": round(per, 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
+                   "num_kv_heads": plan.num_kv_heads, "head_dim": plan.head_dim,
+                   "page_size": plan.page_size, "context": "U[512,4096]",
+                   "kv_bytes_per_step": kv_bytes, "step": "append 1 token/seq + decode",
+                   "l2": "flushed between timed steps (256 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens_s, 1),
+        "pct_of_hbm_peak": round(100.0 * value / (hbm * world), 2),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+        "extra": extra,
+    }
+    return line
+
+
+def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
+    """The other workloads, one number each (same flushing, CUDA graphs)."""
+    res = {}
+    for name in ["shared_prefix", "long_gqa", "long_mqa"]:
+        try:
+            plan = wl.named_plan(name)
+            rig = DecodeRig(plan, dev)
+            g = capture(rig.decode, stream)
+            ms = statistics.mean(timed_graph(g, steps, flush, stream))
+            kvb = wl.decode_kv_bytes(plan)
+            io = wl.decode_io_bytes(plan)
+            ent = {"decode_ms": round(ms, 5), "kv_GBps": round((kvb + io) / (ms * 1e-3) / 1e9, 1),
+                   "frac_hbm": round((kvb + io) / (ms * 1e-3) / 1e9 / hbm, 4),
+                   "tokens_per_s": round(plan.batch / (ms * 1e-3), 1)}
+            if name == "shared_prefix":
+                ub = wl.decode_unique_kv_bytes(plan)
+                ent["unique_kv_GBps"] = round(ub / (ms * 1e-3) / 1e9, 1)
+                ent["unique_frac_hbm"] = round(ub / (ms * 1e-3) / 1e9 / hbm, 4)
+            res[name] = ent
+            del rig, g
+            torch.cuda.empty_cache()
+        except Exception as ex:  # report, do not hide
+            res[name] = {"error": repr(ex)[:200]}
+    try:
+        plan = wl.named_plan("chunked_prefill")
+        rig = PrefillRig(plan, dev)
+        g = capture(rig.prefill, stream)
+        ms = statistics.mean(timed_graph(g, steps, flush, stream))
+        ga = capture(rig.append, stream)
+        ams = statistics.mean(timed_graph(ga, steps, flush, stream))
+        fl = wl.prefill_flops(plan)
+        tf = fl / (ms * 1e-3) / 1e12
+        ab = wl.append_bytes(plan)
+        res["chunked_prefill"] = {
+            "prefill_ms": round(ms, 4), "TFLOPs": round(tf, 1),
+            "frac_bf16_burst": round(tf / bf16, 4), "frac_bf16_sustained": round(tf / bf16_sus, 4),
+            "visible_pairs": wl.prefill_visible_pairs(plan), "flops": fl,
+            "append_ms": round(ams, 5), "append_GBps": round(ab / (ams * 1e-3) / 1e9, 1),
+            "append_frac_hbm": round(ab / (ams * 1e-3) / 1e9 / hbm, 4)}
+    except Exception as ex:
+        res["chunked_prefill"] = {"error": repr(ex)[:200]}
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    plan = wl.named_plan(args.workload)
+    rig = OracleRig(plan, 4)   # each step: a bounded sample of the workload
+    for _ in range(args.warmup):
+        rig.step()
+    pers = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        rig.step()
+        pers.append(time.perf_counter() - t0)
+    el = time.perf_counter() - t_all
+    per = statistics.mean(pers)
+    value = rig.kv_bytes / per / 1e9
+    cores = cpu_cores()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
+                   "num_kv_heads": plan.num_kv_heads, "head_dim": plan.head_dim,
+                   "page_size": plan.page_size, "sample_sequences": rig.k},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": rig.describe(len(pers), el)},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; other ranks exit at once without work
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup()
+    line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * paged_attn.h -- C ABI of libpagedattn.so: paged (block-table) KV-cache
+ * append and attention on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the I/O contract of onnxruntime/mobius PR #395
+ * "Add paged / block-table KV cache export" (sections "How it works (per
+ * attention layer)" and "ONNX I/O contract"): new K/V rows are scattered
+ * into a per-layer page pool at slot_mapping (ScatterND), and attention
+ * reads a sequence's pages through block_table (Gather) with causal and
+ * padding masking given by nonpad_kv_seqlen (here: seq_lens).  The batched,
+ * row-padded block_table, seq_lens and query_start_loc follow the vLLM-shaped
+ * metadata of ROCm/maxtext PR #93 "[Draft] kv paged kernels" (the
+ * attention='gpu_paged' commit).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *   owned by the caller.  The library allocates no device memory and keeps
+ *   no per-call state; the only library state is one device-side error
+ *   word per device (see paged_device_error).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream).  Host-side argument checks run before any launch; on a
+ *   non-PA_OK return nothing was launched.
+ * - Pool layout (NHD): key_pool and value_pool are each
+ *   [num_pages, page_size, num_kv_heads, head_dim], contiguous, element type
+ *   `dtype`.  The flat slot s = page_id * page_size + offset addresses row s
+ *   of the pool viewed as [num_pages * page_size, num_kv_heads, head_dim].
+ * - GQA/MQA: num_q_heads must be a multiple of num_kv_heads; query head h
+ *   reads KV head h / (num_q_heads / num_kv_heads).
+ * - The softmax scale is a required argument (there is no default 1/sqrt(d)):
+ *   a query that already carries its scale is passed with scale = 1.0.
+ * - There is no attention-bias, ALiBi or sliding-window argument: those are
+ *   unsupported, not silently ignored.
+ * - Device-side checks: a block_table entry outside [0, num_pages), a slot
+ *   >= num_pages * page_size, or a seq_len outside [0, max_blocks_per_seq *
+ *   page_size] is recorded in the device error word and the offending read
+ *   or write is skipped (no trap, no hang).
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,         /* a required pointer is NULL                        */
+  PA_ERR_SHAPE = 2,        /* inconsistent or negative sizes                    */
+  PA_ERR_DTYPE = 3,        /* unknown dtype                                     */
+  PA_ERR_RANGE = 4,        /* a size is beyond what the kernels index (int32)   */
+  PA_ERR_UNSUPPORTED = 5,  /* valid but not implemented (head_dim, page_size)   */
+  PA_ERR_CUDA = 6,         /* a CUDA runtime call failed (launch, attribute)    */
+  PA_ERR_WORKSPACE = 7,    /* workspace missing or smaller than required        */
+  PA_ERR_ALIGN = 8         /* a pointer is not aligned as the dtype requires    */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_DTYPE_F32 = 0,        /* float32 pool, q and out                           */
+  PA_DTYPE_BF16 = 1        /* bfloat16 pool, q and out; fp32 accumulation       */
+} pa_dtype;
+
+/* One layer's KV page pool (mobius PR #395 "ONNX I/O contract":
+ * key_pool.{i} / value_pool.{i}).  All fields are read-only to the library
+ * except the pool contents, which paged_kv_append updates in place. */
+typedef struct pa_kv_pool {
+  void* key_pool;          /* device [num_pages, page_size, num_kv_heads, head_dim] */
+  void* value_pool;        /* device, same shape and dtype                           */
+  int64_t num_pages;       /* > 0; num_pages * page_size < 2^31                      */
+  int32_t page_size;       /* tokens per page, > 0                                   */
+  int32_t num_kv_heads;    /* > 0                                                    */
+  int32_t head_dim;        /* > 0                                                    */
+  int32_t dtype;           /* pa_dtype                                               */
+} pa_kv_pool;
+
+/*
+ * paged_kv_append -- the ScatterND write (mobius PR #395, "How it works",
+ * step 1; the aiter AppendKvJA step of maxtext PR #93).
+ *
+ *   for t in [0, num_tokens):  if slot_mapping[t] >= 0:
+ *       key_pool.flat[slot_mapping[t]]   = key[t]
+ *       value_pool.flat[slot_mapping[t]] = value[t]
+ *
+ * key, value    device [num_tokens, num_kv_heads, head_dim], pool dtype.
+ * slot_mapping  device int64 [num_tokens]; entry = page_id * page_size +
+ *               offset.  A negative entry marks a padding token (skipped).
+ *               Entries must be unique within one call (otherwise which
+ *               row lands is unspecified).  An entry >= num_pages*page_size
+ *               is recorded in the device error word and skipped.
+ * num_tokens    >= 0; 0 launches nothing.
+ * The write is a bit copy: the pool afterwards is bit-identical to the
+ * ScatterND result.
+ */
+pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* value,
+                          const int64_t* slot_mapping, int64_t num_tokens, void* stream);
+
+/*
+ * paged_attention_decode -- one query token per sequence, attending to all
+ * seq_lens[b] keys of its pages (mobius PR #395: Gather(pool, block_table)
+ * then Attention with nonpad_kv_seqlen; decode is the one-token case).
+ *
+ *   out[b, h] = sum_j softmax_j(scale * q[b,h] . K_b[j, h/G]) V_b[j, h/G],
+ *   j in [0, seq_lens[b]),  K_b[j] = key_pool[block_table[b, j / page_size],
+ *                                             j % page_size]
+ *
+ * q, out        device [batch, num_q_heads, head_dim], pool dtype.  out may
+ *               not alias q.  A sequence with seq_lens[b] == 0 gets out = 0.
+ * block_table   device int32 [batch, max_blocks_per_seq], row-padded; entries
+ *               past ceil(seq_lens[b] / page_size) are never read.
+ * seq_lens      device int32 [batch], the KV length including this step's
+ *               appended token (append first, then attend).
+ * max_seq_len   host upper bound of seq_lens (used to size the launch).
+ * workspace     device scratch of at least
+ *               paged_attention_decode_workspace_size(...) bytes (may be NULL
+ *               when that size is 0), 16-byte aligned, owned by the caller and
+ *               not shared by calls in flight at the same time.
+ * bf16 path: head_dim in {64, 128}, page_size a power of two;
+ * f32 path: head_dim <= 256, any page_size.
+ */
+size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim,
+                                             int32_t dtype);
+
+pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out,
+                                 int32_t batch, int32_t num_q_heads,
+                                 const int32_t* block_table, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * paged_attention_prefill -- varlen causal attention for a packed batch of
+ * new tokens (query_start_loc layout of maxtext PR #93's vLLM-shaped
+ * metadata; causal + padding masks from is_causal=1 and nonpad_kv_seqlen of
+ * mobius PR #395).
+ *
+ * Sequence b owns packed rows [query_start_loc[b], query_start_loc[b+1]) of
+ * q; with n_b rows and L_b = seq_lens[b], its row i is the token at absolute
+ * position p = L_b - n_b + i and attends to keys 0..p of its pages (the new
+ * tokens are the last n_b of the sequence, already appended).  A row with
+ * p < 0 gets out = 0.
+ *
+ * q, out           device [total_q, num_q_heads, head_dim], pool dtype.
+ * query_start_loc  device int32 [batch + 1], non-decreasing, [0] = 0,
+ *                  [batch] = total_q.
+ * max_q_len        host upper bound of n_b (sizes the launch).
+ * block_table, seq_lens, max_seq_len, scale: as for decode.
+ * bf16 path: head_dim in {64, 128}, page_size a power of two;
+ * f32 path: head_dim <= 256.
+ */
+pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out,
+                                  int32_t batch, int32_t num_q_heads,
+                                  const int32_t* query_start_loc, int64_t total_q,
+                                  int32_t max_q_len, const int32_t* block_table,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t max_seq_len, float scale, void* stream);
+
+/*
+ * paged_device_error -- read and clear the device error word of the current
+ * device.  Synchronises the device.  *code = 0 when no violation was seen,
+ * else 1 = block_table entry out of range, 2 = slot out of range,
+ * 3 = seq_len out of range, 4 = query_start_loc inconsistent; *detail holds
+ * the offending value.  Either pointer may be NULL.
+ */
+pa_status paged_device_error(int64_t* code, int64_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* pa_status_string(int32_t status);
+
+/* PA_ABI_VERSION of the loaded library. */
+int32_t pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

@@ -1,0 +1,292 @@
+// C ABI of libpagedattn.so (declared in include/paged_attn.h): host-side
+// argument checks, launch-shape choices and dispatch to the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/paged_attn.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One error word per device, written by kernels on a range violation.
+__device__ unsigned long long g_error_word;
+
+std::atomic<unsigned long long*> g_err_ptr[kMaxDevices];
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+unsigned long long* error_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  unsigned long long* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+
+pa_status check_pool(const pa_kv_pool* pool) {
+  if (pool == nullptr || pool->key_pool == nullptr || pool->value_pool == nullptr) return PA_ERR_NULL;
+  if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16) return PA_ERR_DTYPE;
+  if (pool->num_pages <= 0 || pool->page_size <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0)
+    return PA_ERR_SHAPE;
+  if (pool->num_pages > INT32_MAX) return PA_ERR_RANGE;
+  const size_t es = elem_size(pool->dtype);
+  if (!aligned(pool->key_pool, es) || !aligned(pool->value_pool, es)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+pa::PoolGeom geom(const pa_kv_pool* pool) {
+  pa::PoolGeom g;
+  g.key_pool = pool->key_pool;
+  g.value_pool = pool->value_pool;
+  g.num_pages = pool->num_pages;
+  g.page_size = pool->page_size;
+  g.page_shift = is_pow2(pool->page_size) ? pa::ilog2_pow2(pool->page_size) : -1;
+  g.num_kv_heads = pool->num_kv_heads;
+  g.head_dim = pool->head_dim;
+  return g;
+}
+
+// Shape checks common to decode and prefill.
+pa_status check_attention(const pa_kv_pool* pool, int32_t batch, int32_t num_q_heads,
+                          int32_t max_blocks_per_seq, int32_t max_seq_len, float scale) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0) return PA_ERR_SHAPE;
+  if (num_q_heads % pool->num_kv_heads != 0) return PA_ERR_SHAPE;
+  if ((int64_t)max_blocks_per_seq * pool->page_size > INT32_MAX) return PA_ERR_RANGE;
+  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->page_size) return PA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return PA_ERR_RANGE;
+  if (pool->dtype == PA_DTYPE_BF16) {
+    if (pool->head_dim != 64 && pool->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!is_pow2(pool->page_size)) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads / pool->num_kv_heads > 32) return PA_ERR_UNSUPPORTED;
+    if (!aligned(pool->key_pool, 16) || !aligned(pool->value_pool, 16)) return PA_ERR_ALIGN;
+  } else {
+    if (pool->head_dim > 256) return PA_ERR_UNSUPPORTED;
+  }
+  return PA_OK;
+}
+
+constexpr double kLog2e = 1.4426950408889634;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t decode_ws_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int ctas) {
+  if (batch <= 0 || hq <= 0 || hkv <= 0 || d <= 0) return 0;
+  const int64_t slots = pa::decode_partial_slots(batch, hkv, ctas);
+  const int64_t g = hq / hkv;
+  return align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char* pa_status_string(int32_t status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: inconsistent or negative sizes";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: unknown dtype";
+    case PA_ERR_RANGE: return "PA_ERR_RANGE: a value is outside the supported range";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head_dim/page_size/group not implemented";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA runtime call failed";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: a pointer is misaligned";
+    default: return "unknown pa_status";
+  }
+}
+
+pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* value,
+                          const int64_t* slot_mapping, int64_t num_tokens, void* stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (key == nullptr || value == nullptr || slot_mapping == nullptr) return PA_ERR_NULL;
+  if (!aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
+  const size_t es = elem_size(pool->dtype);
+  pa::AppendParams p;
+  p.key_pool = pool->key_pool;
+  p.value_pool = pool->value_pool;
+  p.key = key;
+  p.value = value;
+  p.slot_mapping = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.num_slots = pool->num_pages * (int64_t)pool->page_size;
+  p.row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * (int64_t)es;
+  p.err = error_word();
+  int vec = 16;
+  while (vec > (int)es && ((p.row_bytes % vec) != 0 || !aligned(key, vec) || !aligned(value, vec) ||
+                           !aligned(pool->key_pool, vec) || !aligned(pool->value_pool, vec)))
+    vec >>= 1;
+  if (!aligned(key, es) || !aligned(value, es)) return PA_ERR_ALIGN;
+  cudaError_t e = pa::launch_append(p, vec, num_sms(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t dtype) {
+  if (dtype != PA_DTYPE_BF16) return 0;
+  return decode_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_sms());
+}
+
+pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                 int32_t num_q_heads, const int32_t* block_table,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float scale, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  pa_status st = check_attention(pool, batch, num_q_heads, max_blocks_per_seq, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (batch == 0) return PA_OK;
+  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr) return PA_ERR_NULL;
+  if (q == out) return PA_ERR_SHAPE;
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return PA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const pa::PoolGeom g = geom(pool);
+  const int32_t group = num_q_heads / pool->num_kv_heads;
+  if (pool->dtype == PA_DTYPE_F32) {
+    if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+    pa::AttnF32Params p;
+    p.pool = g;
+    p.q = static_cast<const float*>(q);
+    p.out = static_cast<float*>(out);
+    p.query_start_loc = nullptr;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.rows = batch;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale = scale;
+    p.err = error_word();
+    return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, pool->head_dim,
+                                       group);
+  const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
+  const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas);
+  pa::DecodeParams p;
+  p.pool = g;
+  p.q = q;
+  p.out = out;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                        align_up((size_t)(slots * group * pool->head_dim * 4), 256));
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.group = group;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_ctas = ctas;
+  p.scale_log2 = (float)((double)scale * kLog2e);
+  p.err = error_word();
+  return pa::launch_decode_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                  int32_t num_q_heads, const int32_t* query_start_loc, int64_t total_q,
+                                  int32_t max_q_len, const int32_t* block_table,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t max_seq_len, float scale, void* stream) {
+  pa_status st = check_attention(pool, batch, num_q_heads, max_blocks_per_seq, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (total_q < 0 || max_q_len < 0 || total_q > INT32_MAX) return PA_ERR_SHAPE;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  if (max_q_len == 0) return PA_ERR_SHAPE;
+  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      query_start_loc == nullptr)
+    return PA_ERR_NULL;
+  if (q == out) return PA_ERR_SHAPE;
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return PA_ERR_ALIGN;
+  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const pa::PoolGeom g = geom(pool);
+  const int32_t group = num_q_heads / pool->num_kv_heads;
+  if (pool->dtype == PA_DTYPE_F32) {
+    pa::AttnF32Params p;
+    p.pool = g;
+    p.q = static_cast<const float*>(q);
+    p.out = static_cast<float*>(out);
+    p.query_start_loc = query_start_loc;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.rows = total_q;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale = scale;
+    p.err = error_word();
+    return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  pa::PrefillParams p;
+  p.pool = g;
+  p.q = q;
+  p.out = out;
+  p.query_start_loc = query_start_loc;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.total_q = total_q;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.group = group;
+  p.max_blocks = max_blocks_per_seq;
+  p.max_q_len = max_q_len;
+  p.scale_log2 = (float)((double)scale * kLog2e);
+  p.err = error_word();
+  return pa::launch_prefill_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status paged_device_error(int64_t* code, int64_t* detail) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  unsigned long long w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)) != cudaSuccess) return PA_ERR_CUDA;
+  const unsigned long long zero = 0;
+  if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return PA_ERR_CUDA;
+  if (code) *code = (int64_t)(w >> 56);
+  if (detail) {
+    int64_t d = (int64_t)(w & ((1ull << 56) - 1));
+    if (d & (1ll << 55)) d -= (1ll << 56);  // sign-extend the 56-bit field
+    *detail = d;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// fp32 path of paged_attention_decode / paged_attention_prefill.
+//
+// Same operation as the bf16 kernels (onnxruntime/mobius PR #395 "Add paged /
+// block-table KV cache export", "How it works": Gather through block_table,
+// then attention with is_causal + nonpad_kv_seqlen masking), computed in
+// fp32 on CUDA cores so that an fp32 pool keeps fp32 accuracy end to end.
+// One warp owns one (query row, query head); lanes split head_dim (up to
+// 256), keys are visited one at a time with an online softmax.  This path
+// serves small fp32 models and correctness runs, not the bf16 hot path.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMaxPerLane = 8;  // head_dim <= 256
+
+__global__ void __launch_bounds__(256) attn_f32_kernel(AttnF32Params p) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = blockDim.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * warps_per_block;
+  const int D = p.pool.head_dim, Hq = p.num_q_heads, Hkv = p.pool.num_kv_heads;
+  const int ps = p.pool.page_size;
+  const int max_len = p.max_blocks * ps;
+  const int64_t total = p.rows * Hq;
+  const float* kpool = static_cast<const float*>(p.pool.key_pool);
+  const float* vpool = static_cast<const float*>(p.pool.value_pool);
+  for (int64_t w = (int64_t)blockIdx.x * warps_per_block + (threadIdx.x >> 5); w < total; w += nwarps) {
+    const int64_t r = w / Hq;
+    const int h = (int)(w - r * Hq);
+    const int hk = h / p.group;
+    int b, n, i;
+    if (p.query_start_loc == nullptr) {
+      b = (int)r; n = 1; i = 0;
+    } else {
+      int lo = 0, hi = p.batch;  // largest b with query_start_loc[b] <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.query_start_loc + mid) <= r) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const int s0 = __ldg(p.query_start_loc + b);
+      n = __ldg(p.query_start_loc + b + 1) - s0;
+      i = (int)(r - s0);
+    }
+    int L = __ldg(p.seq_lens + b);
+    if (L < 0 || L > max_len) {
+      if (lane == 0) record_error(p.err, ERR_SEQ_LEN, L);
+      L = L < 0 ? 0 : max_len;
+    }
+    const int pos = L - n + i;
+    const float* qrow = p.q + (r * Hq + h) * (int64_t)D;
+    float qv[kMaxPerLane], ov[kMaxPerLane];
+#pragma unroll
+    for (int t = 0; t < kMaxPerLane; ++t) {
+      const int d = lane + 32 * t;
+      qv[t] = d < D ? qrow[d] : 0.f;
+      ov[t] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
+    for (int j = 0; j <= pos; ++j) {
+      const int page = __ldg(bt + j / ps);
+      if (page < 0 || page >= p.pool.num_pages) {
+        if (lane == 0) record_error(p.err, ERR_BLOCK_TABLE, page);
+        continue;
+      }
+      const int64_t off = ((int64_t)page * ps + j % ps) * Hkv * D + (int64_t)hk * D;
+      float s = 0.f;
+#pragma unroll
+      for (int t = 0; t < kMaxPerLane; ++t) {
+        const int d = lane + 32 * t;
+        if (d < D) s = fmaf(qv[t], kpool[off + d], s);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      s *= p.scale;
+      const float mn = fmaxf(m, s);
+      const float a = expf(m - mn);
+      const float e = expf(s - mn);
+      l = l * a + e;
+#pragma unroll
+      for (int t = 0; t < kMaxPerLane; ++t) {
+        const int d = lane + 32 * t;
+        if (d < D) ov[t] = fmaf(ov[t], a, e * vpool[off + d]);
+      }
+      m = mn;
+    }
+    float* orow = p.out + (r * Hq + h) * (int64_t)D;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxPerLane; ++t) {
+      const int d = lane + 32 * t;
+      if (d < D) orow[d] = ov[t] * inv;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const AttnF32Params& p, int num_sms, cudaStream_t s) {
+  const int64_t total = p.rows * p.num_q_heads;
+  if (total <= 0) return cudaSuccess;
+  const int threads = 256, wpb = threads / 32;
+  int64_t blocks = (total + wpb - 1) / wpb;
+  if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+  attn_f32_kernel<<<(int)blocks, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,94 @@
+// Device helpers shared by the paged-attention kernels (sm_103a).
+// Inline PTX wrappers for cp.async, ldmatrix and the warp-level bf16 MMA,
+// plus the device error word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Device error word: high 8 bits = code, low 56 bits = detail.  The first
+// violation wins; later ones are dropped.  Never traps.
+enum : unsigned long long {
+  ERR_BLOCK_TABLE = 1,
+  ERR_SLOT = 2,
+  ERR_SEQ_LEN = 3,
+  ERR_QUERY_LOC = 4,
+};
+
+__device__ __forceinline__ void record_error(unsigned long long* err, unsigned long long code,
+                                             long long detail) {
+  if (err == nullptr) return;
+  unsigned long long packed = (code << 56) | ((unsigned long long)detail & ((1ull << 56) - 1));
+  atomicCAS(err, 0ull, packed);
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16-byte, L2-only) with zero fill when src_bytes == 0.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// ldmatrix / mma.sync m16n8k16 bf16 -> fp32
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// Swizzled byte offset of 16-byte chunk `chunk` of row `row` in a tile whose
+// rows are `row_bytes` long (row_bytes a multiple of 128): the chunk index is
+// XOR-ed with (row % 8) so that 8 rows read at one logical chunk hit 8
+// distinct bank groups (ldmatrix is then conflict-free).
+__device__ __forceinline__ uint32_t swz(int row, int chunk, int row_bytes) {
+  return row * row_bytes + ((chunk ^ (row & 7)) << 4);
+}
+
+__host__ __device__ __forceinline__ int ilog2_pow2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+}  // namespace pa

@@ -1,0 +1,94 @@
+// Launch-side declarations shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Geometry of one layer's pool, as the kernels see it.
+struct PoolGeom {
+  const void* key_pool;
+  const void* value_pool;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t page_shift;     // log2(page_size) when page_size is a power of two, else -1
+  int32_t num_kv_heads;
+  int32_t head_dim;
+};
+
+// ---- append ---------------------------------------------------------------
+struct AppendParams {
+  void* key_pool;
+  void* value_pool;
+  const void* key;
+  const void* value;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int64_t num_slots;      // num_pages * page_size
+  int64_t row_bytes;      // num_kv_heads * head_dim * elem_size
+  unsigned long long* err;
+};
+cudaError_t launch_append(const AppendParams& p, int vec_bytes, int num_sms, cudaStream_t s);
+
+// ---- decode (bf16, split-KV over a balanced partition of 16-key blocks) ---
+struct DecodeParams {
+  PoolGeom pool;
+  const void* q;          // [B, Hq, D] bf16
+  void* out;              // [B, Hq, D] bf16
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* part_o;          // [slots, G, D] fp32 unnormalised partial outputs
+  float2* part_ml;        // [slots, G] (running max in log2 units, denominator)
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t group;          // G = Hq / Hkv
+  int32_t max_blocks;     // block_table row length
+  int32_t num_ctas;       // CTAs of the split kernel (partition count)
+  float scale_log2;       // scale * log2(e)
+  unsigned long long* err;
+};
+// Number of partial slots the split kernel may write for this launch.
+int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas);
+int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
+                    int32_t head_dim, int32_t group);
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
+
+// ---- prefill (bf16) ------------------------------------------------------
+struct PrefillParams {
+  PoolGeom pool;
+  const void* q;          // [T, Hq, D] bf16
+  void* out;              // [T, Hq, D] bf16
+  const int32_t* query_start_loc;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int64_t total_q;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t group;
+  int32_t max_blocks;
+  int32_t max_q_len;
+  float scale_log2;
+  unsigned long long* err;
+};
+cudaError_t launch_prefill_bf16(const PrefillParams& p, cudaStream_t s);
+
+// ---- fp32 path (decode = prefill with one row per sequence) --------------
+struct AttnF32Params {
+  PoolGeom pool;
+  const float* q;         // [rows, Hq, D]
+  float* out;
+  const int32_t* query_start_loc;  // null for decode (row b = sequence b, n_b = 1)
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int64_t rows;
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t group;
+  int32_t max_blocks;
+  float scale;
+  unsigned long long* err;
+};
+cudaError_t launch_attn_f32(const AttnF32Params& p, int num_sms, cudaStream_t s);
+
+}  // namespace pa

@@ -1,0 +1,105 @@
+"""The C ABI: the library builds, loads, and exports every declared symbol;
+host-side argument checks return the documented status codes.  No kernel
+is launched here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from serving_slot_mapping_gb300 import build as build_mod
+from serving_slot_mapping_gb300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "paged_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return capi.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("paged_kv_append", "paged_attention_decode", "paged_attention_prefill"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(L, n), f"missing export {n}"
+        assert n in capi.SIGNATURES, f"binding does not declare {n}"
+
+
+def test_abi_version(L):
+    assert L.pa_abi_version() == 1
+    assert b"PA_ERR_SHAPE" in L.pa_status_string(2)
+
+
+def _pool(dtype=capi.PA_DTYPE_BF16, hkv=8, d=128, ps=16, P=64, k=0x10000, v=0x20000):
+    return capi.PaKvPool(k, v, P, ps, hkv, d, dtype)
+
+
+FAKE = ctypes.c_void_p(0x40000)  # never dereferenced: every call below fails validation
+
+
+def test_append_validation(L):
+    assert L.paged_kv_append(None, FAKE, FAKE, FAKE, 4, None) == capi.PA_ERR_NULL
+    p = _pool(dtype=7)
+    assert L.paged_kv_append(ctypes.byref(p), FAKE, FAKE, FAKE, 4, None) == capi.PA_ERR_DTYPE
+    p = _pool(P=0)
+    assert L.paged_kv_append(ctypes.byref(p), FAKE, FAKE, FAKE, 4, None) == capi.PA_ERR_SHAPE
+    p = _pool()
+    assert L.paged_kv_append(ctypes.byref(p), FAKE, FAKE, FAKE, -1, None) == capi.PA_ERR_SHAPE
+    assert L.paged_kv_append(ctypes.byref(p), None, FAKE, FAKE, 4, None) == capi.PA_ERR_NULL
+    assert L.paged_kv_append(ctypes.byref(p), FAKE, FAKE, ctypes.c_void_p(0x40004), 4,
+                             None) == capi.PA_ERR_ALIGN
+    # zero tokens: nothing to do, no launch
+    assert L.paged_kv_append(ctypes.byref(p), None, None, None, 0, None) == capi.PA_OK
+
+
+def _decode(L, pool, hq=32, batch=2, mb=4, msl=64, scale=0.1, ws=None, wsb=0, q=FAKE, out=None):
+    return L.paged_attention_decode(ctypes.byref(pool), q, out or ctypes.c_void_p(0x50000), batch, hq,
+                                    FAKE, mb, FAKE, msl, scale, ws, wsb, None)
+
+
+def test_decode_validation(L):
+    assert _decode(L, _pool(), hq=12) == capi.PA_ERR_SHAPE          # 12 % 8 != 0
+    assert _decode(L, _pool(d=96)) == capi.PA_ERR_UNSUPPORTED       # bf16 head_dim
+    assert _decode(L, _pool(ps=12), msl=40) == capi.PA_ERR_UNSUPPORTED  # bf16 page_size
+    assert _decode(L, _pool(hkv=1), hq=64) == capi.PA_ERR_UNSUPPORTED  # group 64
+    assert _decode(L, _pool(), scale=float("nan")) == capi.PA_ERR_RANGE
+    assert _decode(L, _pool(), msl=65) == capi.PA_ERR_SHAPE          # > max_blocks * page_size
+    assert _decode(L, _pool(), q=None) == capi.PA_ERR_NULL
+    assert _decode(L, _pool(), out=FAKE) == capi.PA_ERR_SHAPE        # out aliases q
+    assert _decode(L, _pool(), batch=0) == capi.PA_OK
+    assert _decode(L, _pool(k=0x10008)) == capi.PA_ERR_ALIGN         # bf16 pool needs 16 B
+    assert _decode(L, _pool(), ws=None, wsb=0) == capi.PA_ERR_WORKSPACE
+
+
+def test_prefill_validation(L):
+    p = _pool()
+    f = L.paged_attention_prefill
+    assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 0, FAKE, 4, FAKE, 64,
+             0.1, None) == capi.PA_ERR_SHAPE                      # max_q_len 0 with tokens
+    assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, None, 10, 5, FAKE, 4, FAKE, 64,
+             0.1, None) == capi.PA_ERR_NULL
+    assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 0, 5, FAKE, 4, FAKE, 64,
+             0.1, None) == capi.PA_OK                             # nothing to do
+    assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4, FAKE, 64,
+             float("inf"), None) == capi.PA_ERR_RANGE
+
+
+def test_workspace_size_is_zero_for_f32_and_positive_for_bf16(L):
+    assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_F32) == 0
+    assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_BF16) > 0
