@@ -133,6 +133,40 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode_static_scratch -- paged_attention_decode without a
+ * caller-provided workspace.  The pages have no counterpart of this call: it
+ * exists for callers that cannot allocate device memory, such as a plugin in
+ * an inference runtime that owns all device memory and hands its plugins no
+ * allocator, or a latency-critical serving loop that may not take
+ * cudaMalloc's implicit synchronisation mid-step.
+ *
+ * The split-KV partials go to a file-scope device array of
+ * PA_DECODE_STATIC_SCRATCH_BYTES that the library holds on every GPU that
+ * loads it, until the process exits.  The call allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ * - The first call on a device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress); make that first call before
+ *   any stream capture on the device.
+ * - All calls share the one array, which keeps the last call's contents;
+ *   calls whose kernels overlap on the GPU (different streams, or unordered
+ *   host threads) race on it.  Nothing in it needs to start zeroed.
+ * - bf16 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
+ *   workspace anyway).  A call whose partials would not fit, i.e. when
+ *   paged_attention_decode_workspace_size(...) exceeds
+ *   PA_DECODE_STATIC_SCRATCH_BYTES, returns PA_ERR_WORKSPACE and launches
+ *   nothing.
+ * Arguments, layout and results are those of paged_attention_decode.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+
+pa_status paged_attention_decode_static_scratch(const pa_kv_pool* pool, const void* q, void* out,
+                                                int32_t batch, int32_t num_q_heads,
+                                                const int32_t* block_table,
+                                                int32_t max_blocks_per_seq,
+                                                const int32_t* seq_lens, int32_t max_seq_len,
+                                                float scale, void* stream);
+
+/*
  * paged_attention_prefill -- varlen causal attention for a packed batch of
  * new tokens (query_start_loc layout of maxtext PR #93's vLLM-shaped
  * metadata; causal + padding masks from is_causal=1 and nonpad_kv_seqlen of

@@ -20,7 +20,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "prefill_bf16.cu", "attn_f32.cu"]
+SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "prefill_bf16.cu", "attn_f32.cu",
+           "decode_noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -45,6 +45,9 @@ SIGNATURES = {
     "paged_attention_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "paged_attention_decode": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i32,
                                       _c_void_p, _i32, _f32, _c_void_p, _sz, _c_void_p]),
+    "paged_attention_decode_static_scratch": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32,
+                                                     _c_void_p, _i32, _c_void_p, _i32, _f32,
+                                                     _c_void_p]),
     "paged_attention_prefill": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i64,
                                        _i32, _c_void_p, _i32, _c_void_p, _i32, _f32, _c_void_p]),
     "paged_device_error": (_i32, [ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -178,6 +181,32 @@ def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale
                                       _ptr(block_table), mb, _ptr(seq_lens), int(max_seq_len),
                                       float(scale), _ptr(workspace), wbytes, _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_static_scratch(key_pool, value_pool, q, block_table, seq_lens, scale,
+                                          max_seq_len=None, out=None, stream=None):
+    """Decode attention whose scratch is the library's own static device array.
+
+    For callers that may not allocate device memory; see the header for the
+    size limit and the sharing rules of that array.
+    """
+    pool = make_pool(key_pool, value_pool)
+    _contig(q, "q")
+    _contig(block_table, "block_table")
+    B, hq, d = q.shape
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    mb = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = mb * pool.page_size
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib().paged_attention_decode_static_scratch(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
+                                                     _ptr(block_table), mb, _ptr(seq_lens),
+                                                     int(max_seq_len), float(scale),
+                                                     _stream(stream))
+    _check(st, "paged_attention_decode_static_scratch")
     return out
 
 
