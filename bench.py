@@ -56,7 +56,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_decode")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle CPU-baseline sample length; <= 0 skips it")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     return ap.parse_args()
 
 
@@ -426,18 +428,20 @@ def run_ours(args, rank, world, local):
                 "algorithmic_bytes_per_launch": dec_bytes,
                 "ms_per_launch": round(dec_ms, 5), "peak_source": peak_src}
 
-    e2e_ms, h2d, d2h = e2e_decode(rig, max(20, min(args.steps, 200)), flush)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    e2e = {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_ms, 5)}
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_decode(rig, max(20, min(args.steps, 200)), flush)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": round(total_kv / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 5)}
 
     extra = {}
     if not args.no_extra and rank == 0:
         extra = run_extra(dev, flush, stream, hbm, bf16, bf16_sus)
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         gbs, per, desc = cpu_oracle_decode(plan, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": desc, "s_per_step": round(per, 4)}

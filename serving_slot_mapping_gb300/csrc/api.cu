@@ -46,6 +46,13 @@ int num_sms() {
   return n;
 }
 
+int max_smem_optin() {
+  const int dev = current_device();
+  int v = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return v;
+}
+
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -194,12 +201,14 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
     p.err = error_word();
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
-  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  if (pool->page_size < 8) return PA_ERR_UNSUPPORTED;  // TMA boxes of >= 8 rows
+  if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
   const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, pool->head_dim,
                                        group);
   const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
+  if (pa::decode_smem_bytes(pool->head_dim, group, batch) > (size_t)max_smem_optin()) return PA_ERR_UNSUPPORTED;
   const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas);
   pa::DecodeParams p;
   p.pool = g;

@@ -12,31 +12,32 @@
 //   list is cut into `num_ctas` equal contiguous ranges (one persistent CTA
 //   per SM).  Every CTA streams the same number of KV bytes whatever the mix
 //   of context lengths, so there is no tail of idle SMs.
-// * A CTA walks its range pair by pair ("segments").  NWK warps take NWK
-//   consecutive blocks per pipeline stage; RT row-tiles of 16 query heads
-//   cover the G heads that share the KV head, so each page is read from HBM
-//   once for all G heads (GQA/MQA reuse).
-// * Pages are staged with 16-byte cp.async into an XOR-swizzled smem ring of
-//   STAGES stages, following block_table per key row.  Rows at or past L_b
-//   are zero-filled and masked, so stale or NaN-poisoned slots never reach
-//   the arithmetic.
-// * QK^T and PV use mma.sync m16n8k16 bf16 with fp32 accumulation; the
-//   softmax is online in the log2 domain (scale * log2(e) folded in).  The
-//   output rescale is skipped when no running max moved.
-// * A segment that covers a whole pair writes the bf16 output directly.  A
-//   pair cut by a range boundary leaves one fp32 partial (m, l, o) per CTA
-//   in the workspace, and the combine kernel merges them with
+// * Inside a CTA one producer warp walks the range and, for each block,
+//   follows block_table to the page and issues TMA tensor copies of the K and
+//   V rows of that KV head into a ring of mbarrier-guarded stages (128 KB of
+//   KV in flight per SM).  Per pair ("segment") it also bulk-copies the G
+//   query rows that share the KV head.
+// * Consumer warps (key groups x row tiles of 16 query heads) take blocks
+//   round-robin: S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
+//   fp32 accumulate), online softmax in the log2 domain, output rescale
+//   skipped when no running max moved.  Each page is read from HBM once for
+//   all G heads (GQA/MQA reuse).
+// * Keys at or past L_b are masked in S, and their V rows are zeroed in
+//   shared memory, so stale or NaN-poisoned slots never reach the output.
+// * At a segment end the key groups merge in shared memory.  A segment that
+//   covers a whole pair writes the bf16 output directly; a pair cut by a
+//   range boundary leaves one fp32 partial (m, l, o) per CTA in the
+//   workspace, and the combine kernel merges them with
 //   o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
 #include <math.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace pa {
 
 namespace {
-
-constexpr int kNWK = 4;  // warps along keys (blocks per stage)
 
 __device__ __forceinline__ int nblk_of(const int32_t* seq_lens, int b, int max_len,
                                        unsigned long long* err) {
@@ -68,48 +69,85 @@ struct Cursor {
   int64_t u;
 };
 
-template <int D, int RT, int STAGES>
+template <int D, int RT>
 struct Cfg {
-  static constexpr int kThreads = 32 * RT * kNWK;
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kChunks = D / 8;                 // 16-byte chunks per row
-  static constexpr int kBlockBytes = 16 * kRowBytes;    // one 16-key K or V tile
-  static constexpr int kStageBytes = kNWK * 2 * kBlockBytes;
-  static constexpr int kRowsPerStage = kNWK * 2 * 16;
-  static constexpr int kCopiesPerThread = kRowsPerStage * kChunks / kThreads;
+  static constexpr int kNWK = RT == 1 ? 8 : 4;            // key groups
+  static constexpr int kConsumers = kNWK * RT;            // consumer warps
+  static constexpr int kThreads = 32 * (kConsumers + 1);  // + one producer warp
+  static constexpr int kSlabs = D / 64;                   // 128-byte swizzle slabs per row
+  static constexpr int kSlabBytes = 16 * 128;             // one slab of a 16-key tile
+  static constexpr int kTileBytes = kSlabs * kSlabBytes;  // one 16-key K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = D == 128 ? 16 : 32;      // 128 KB of KV in flight per SM
+  static constexpr int kQRows = 16 * RT;
+  static constexpr int kQSlotBytes = kQRows * D * 2;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kBarOffset = kRingBytes + 2 * kQSlotBytes;
+  static constexpr int kNumBars = 2 * kStages + 4;        // full[], empty[], qfull[2], qempty[2]
+  static constexpr int kMergeOffset = kBarOffset + kNumBars * 8;
 };
 
-template <int D, int RT, int STAGES>
-__global__ void __launch_bounds__(32 * RT * kNWK, 1) decode_split_kernel(DecodeParams p) {
-  using C = Cfg<D, RT, STAGES>;
-  extern __shared__ __align__(1024) unsigned char smem[];
+template <int D, int RT>
+size_t split_smem_bytes(int G, int B) {
+  using C = Cfg<D, RT>;
+  return 1024 /* alignment slack */ + (size_t)C::kMergeOffset + (size_t)C::kNWK * G * (D + 2) * 4 +
+         (size_t)(B + 1) * 4;
+}
+
+template <int D, int RT>
+__global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                        DecodeParams p) {
+  using C = Cfg<D, RT>;
+  constexpr int S = C::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int G = p.group;
   const int B = p.batch;
   const int Hkv = p.pool.num_kv_heads;
   const int Hq = p.num_q_heads;
   unsigned char* ring = smem;
-  float* mrg_o = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes);  // [NWK][G][D]
-  float* mrg_ml = mrg_o + kNWK * G * D;                                      // [NWK][G][2]
-  int* prefix = reinterpret_cast<int*>(mrg_ml + kNWK * G * 2);               // [B+1]
+  unsigned char* qring = smem + C::kRingBytes;
+  const uint32_t bars = smem_u32(smem + C::kBarOffset);
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto qfull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
+  auto qempty_bar = [&](int s) { return bars + 8u * (2 * S + 2 + s); };
+  float* mrg_o = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [NWK][G][D]
+  float* mrg_ml = mrg_o + C::kNWK * G * D;                           // [NWK][G][2]
+  int* prefix = reinterpret_cast<int*>(mrg_ml + C::kNWK * G * 2);    // [B+1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wk = warp % kNWK;
-  const int rt = warp / kNWK;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
   const int max_len = p.max_blocks * ps;
 
-  // ---- prefix sum of 16-key block counts over the batch ----
+  // ---- set-up: barriers, zeroed Q slots (rows >= G stay zero), block prefix ----
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), RT);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qfull_bar(s), 1);
+      mbar_init(qempty_bar(s), C::kConsumers);
+    }
+    fence_mbar_init();
+  }
+  for (int i = tid; i < 2 * C::kQSlotBytes / 16; i += C::kThreads)
+    reinterpret_cast<uint4*>(qring)[i] = make_uint4(0, 0, 0, 0);
   for (int b = tid; b < B; b += C::kThreads) prefix[b + 1] = nblk_of(p.seq_lens, b, max_len, p.err);
   if (tid == 0) prefix[0] = 0;
+  fence_proxy_async_smem();
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
     for (int base = 0; base < B; base += 32) {
-      int idx = base + lane;
+      const int idx = base + lane;
       int v = idx < B ? prefix[idx + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int t = __shfl_up_sync(0xffffffffu, v, o);
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += t;
       }
       if (idx < B) prefix[idx + 1] = v + carry;
@@ -129,7 +167,7 @@ __global__ void __launch_bounds__(32 * RT * kNWK, 1) decode_split_kernel(DecodeP
     const int x = (int)(u / Hkv);
     int lo = 0, hi = B;  // largest b in [0, B) with prefix[b] <= x
     while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
+      const int mid = (lo + hi) >> 1;
       if (prefix[mid] <= x) lo = mid; else hi = mid;
     }
     cur.b = lo;
@@ -140,13 +178,6 @@ __global__ void __launch_bounds__(32 * RT * kNWK, 1) decode_split_kernel(DecodeP
     cur.L = seq_len_of(p.seq_lens, cur.b, max_len);
     cur.u = u;
     return cur;
-  };
-  auto stage_len = [&](const Cursor& cur) {
-    int64_t left = u1 - cur.u;
-    int nb = cur.nblk - cur.k;
-    if (nb > kNWK) nb = kNWK;
-    if (left < nb) nb = (int)left;
-    return nb;
   };
   auto advance = [&](Cursor& cur, int nb) {
     cur.u += nb;
@@ -164,114 +195,122 @@ __global__ void __launch_bounds__(32 * RT * kNWK, 1) decode_split_kernel(DecodeP
     }
   };
 
-  const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(p.pool.key_pool);
-  const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(p.pool.value_pool);
-  const int64_t row_elems = (int64_t)Hkv * D;
+  const __nv_bfloat16* qglob = static_cast<const __nv_bfloat16*>(p.q);
 
-  // Issue the cp.async copies of one stage (nb blocks of pair cur) into ring slot `slot`.
-  auto load_stage = [&](const Cursor& cur, int nb, int slot) {
-    unsigned char* st = ring + slot * C::kStageBytes;
-    const int32_t* bt = p.block_table + (int64_t)cur.b * p.max_blocks;
-#pragma unroll
-    for (int i = 0; i < C::kCopiesPerThread; ++i) {
-      const int idx = tid + i * C::kThreads;
-      const int row = idx / C::kChunks;       // [w][tensor][r]
-      const int ch = idx % C::kChunks;
-      const int w = row >> 5, tensor = (row >> 4) & 1, r = row & 15;
-      const int j = (cur.k + w) * 16 + r;
-      bool ok = (w < nb) && (j < cur.L);
-      const __nv_bfloat16* src = kpool;
-      if (ok) {
-        const int page = __ldg(bt + (j >> pshift));
+  if (warp == C::kConsumers) {
+    // ======================= producer warp =======================
+    if (lane != 0) return;
+    const int R = ps < 16 ? ps : 16;  // rows per TMA box (page_size >= 8)
+    Cursor pc = locate(u0);
+    int seg = -1;
+    bool alive = true;
+    for (int64_t i = 0; pc.u < u1; ++i) {
+      if (i == 0 || pc.k == 0) {  // a segment (pair) starts: stage its G query rows
+        ++seg;
+        const int qs = seg & 1;
+        if (seg >= 2 && alive) alive = mbar_wait(qempty_bar(qs), ((seg >> 1) - 1) & 1, p.err);
+        const uint32_t qbytes = (uint32_t)(G * D * 2);
+        mbar_arrive_expect_tx(qfull_bar(qs), qbytes);
+        bulk_load(smem_u32(qring + qs * C::kQSlotBytes),
+                  qglob + ((int64_t)pc.b * Hq + (int64_t)pc.hk * G) * D, qbytes, qfull_bar(qs));
+      }
+      const int slot = (int)(i % S);
+      if (i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
+      const int key0 = pc.k * 16;
+      const int32_t* bt = p.block_table + (int64_t)pc.b * p.max_blocks;
+      int rows[2] = {-1, -1};
+      int nbox = 0;
+      for (int t = 0; t < 16 / R; ++t) {
+        const int kk = key0 + t * R;
+        if (kk >= pc.L) break;
+        const int page = __ldg(bt + (kk >> pshift));
         if (page < 0 || page >= p.pool.num_pages) {
           record_error(p.err, ERR_BLOCK_TABLE, page);
-          ok = false;
-        } else {
-          const int64_t slot_row = ((int64_t)page << pshift) + (j & (ps - 1));
-          src = (tensor ? vpool : kpool) + slot_row * row_elems + (int64_t)cur.hk * D + ch * 8;
+          continue;
+        }
+        rows[t] = page * ps + (kk & (ps - 1));
+        ++nbox;
+      }
+      mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(nbox * 2 * C::kSlabs * R * 128));
+      const uint32_t kdst = smem_u32(ring + slot * C::kStageBytes);
+      const uint32_t vdst = kdst + C::kTileBytes;
+      for (int t = 0; t < 16 / R; ++t) {
+        if (rows[t] < 0) continue;
+#pragma unroll
+        for (int sl = 0; sl < C::kSlabs; ++sl) {
+          tma_load_3d(kdst + sl * C::kSlabBytes + t * R * 128, &tmap_k, sl * 64, pc.hk, rows[t], full_bar(slot));
+          tma_load_3d(vdst + sl * C::kSlabBytes + t * R * 128, &tmap_v, sl * 64, pc.hk, rows[t], full_bar(slot));
         }
       }
-      cp_async_16(smem_u32(st + (w * 2 + tensor) * C::kBlockBytes + swz(r, ch, C::kRowBytes)),
-                  src, ok ? 16 : 0);
+      advance(pc, 1);
     }
-  };
-
-  // ---- prologue: fill STAGES-1 stages ----
-  Cursor pc = locate(u0);
-  int pslot = 0;
-#pragma unroll 1
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (pc.u < u1) {
-      const int nb = stage_len(pc);
-      load_stage(pc, nb, pslot);
-      advance(pc, nb);
-    }
-    cp_async_commit();
-    pslot = (pslot + 1) % STAGES;
+    return;
   }
 
-  Cursor cc = locate(u0);
-  int cslot = 0;
-  bool seg_start = true;
-  int seg_first_k = cc.k;
-
-  // per-warp state: two rows per thread (g = lane/4 and g + 8 of this row tile)
-  uint32_t qf[D / 16][4];
-  float o[D / 8][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // ======================= consumer warps =======================
+  const int rt = warp / C::kNWK;  // row tile: query heads rt*16 .. rt*16+15 of the group
+  const int wk = warp % C::kNWK;  // key group: blocks j with j % kNWK == wk
   const int rA = rt * 16 + (lane >> 2), rB = rA + 8;
   const float sl2 = p.scale_log2;
-
-#pragma unroll 1
+  const int mi = lane >> 3, rr = lane & 7;
+  Cursor cc = locate(u0);
+  int seg = -1;
+  int64_t i0 = 0;  // stage index of the segment's first block
+  bool alive = true;
   while (cc.u < u1) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    // refill the slot consumed in the previous iteration
-    if (pc.u < u1) {
-      const int nb = stage_len(pc);
-      load_stage(pc, nb, pslot);
-      advance(pc, nb);
-    }
-    cp_async_commit();
-    pslot = (pslot + 1) % STAGES;
-
-    const int nb = stage_len(cc);
-    if (seg_start) {
-      seg_start = false;
-      seg_first_k = cc.k;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
-#pragma unroll
-      for (int n8 = 0; n8 < D / 8; ++n8) o[n8][0] = o[n8][1] = o[n8][2] = o[n8][3] = 0.f;
-      const uint32_t* qb = reinterpret_cast<const uint32_t*>(
-          static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)cc.b * Hq + (int64_t)cc.hk * G) * D);
-      const int cpair = (lane & 3);
+    ++seg;
+    const int nb_seg = (int)min((int64_t)(cc.nblk - cc.k), u1 - cc.u);
+    const int first_k = cc.k;
+    // ---- the pair's query rows (A fragments of m16n8k16) ----
+    uint32_t qf[D / 16][4];
+    {
+      const int qs = seg & 1;
+      if (alive) alive = mbar_wait(qfull_bar(qs), (seg >> 1) & 1, p.err);
+      const uint32_t* qsm = reinterpret_cast<const uint32_t*>(qring + qs * C::kQSlotBytes);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int d0 = kk * 16 + cpair * 2;
-        qf[kk][0] = rA < G ? __ldg(qb + (rA * D + d0) / 2) : 0u;
-        qf[kk][1] = rB < G ? __ldg(qb + (rB * D + d0) / 2) : 0u;
-        qf[kk][2] = rA < G ? __ldg(qb + (rA * D + d0 + 8) / 2) : 0u;
-        qf[kk][3] = rB < G ? __ldg(qb + (rB * D + d0 + 8) / 2) : 0u;
+        const int d0 = kk * 16 + (lane & 3) * 2;
+        qf[kk][0] = qsm[(rA * D + d0) >> 1];
+        qf[kk][1] = qsm[(rB * D + d0) >> 1];
+        qf[kk][2] = qsm[(rA * D + d0 + 8) >> 1];
+        qf[kk][3] = qsm[(rB * D + d0 + 8) >> 1];
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty_bar(qs));
     }
+    float o[D / 8][4];
+#pragma unroll
+    for (int n8 = 0; n8 < D / 8; ++n8) o[n8][0] = o[n8][1] = o[n8][2] = o[n8][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    if (wk < nb) {
-      const unsigned char* kt = ring + cslot * C::kStageBytes + (wk * 2) * C::kBlockBytes;
-      const unsigned char* vt = kt + C::kBlockBytes;
+    for (int j = wk; j < nb_seg; j += C::kNWK) {
+      const int64_t stage = i0 + j;
+      const int slot = (int)(stage % S);
+      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((stage / S) & 1), p.err);
+      unsigned char* kt = ring + slot * C::kStageBytes;
+      unsigned char* vt = kt + C::kTileBytes;
+      const int valid = cc.L - (first_k + j) * 16;  // >= 1
+      if (valid < 16) {
+        // rows past L_b may hold stale or poisoned data: zero them in V (K is masked below)
+        for (int e = lane; e < (16 - valid) * C::kSlabs * 8; e += 32) {
+          const int row = valid + e / (C::kSlabs * 8);
+          const int rem = e % (C::kSlabs * 8);
+          *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::kSlabBytes + row * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
       const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
       float s[2][4];
 #pragma unroll
       for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
-      const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + swz((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kRowBytes), b0, b1, b2, b3);
+        ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kSlabBytes), b0, b1, b2, b3);
         mma_bf16_16816(s[0], qf[kk], b0, b1);
         mma_bf16_16816(s[1], qf[kk], b2, b3);
       }
-      const int valid = cc.L - (cc.k + wk) * 16;  // >= 1
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -312,70 +351,61 @@ __global__ void __launch_bounds__(32 * RT * kNWK, 1) decode_split_kernel(DecodeP
       pa[2] = pack_bf16(p_[1][0], p_[1][1]);
       pa[3] = pack_bf16(p_[1][2], p_[1][3]);
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
+      for (int jj = 0; jj < D / 16; ++jj) {
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vbase + swz((mi & 1) * 8 + rr, 2 * j + (mi >> 1), C::kRowBytes), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * j], pa, b0, b1);
-        mma_bf16_16816(o[2 * j + 1], pa, b2, b3);
+        ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kSlabBytes), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * jj], pa, b0, b1);
+        mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
       }
+      if (valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(slot));
     }
 
-    const bool pair_end = (cc.k + nb == cc.nblk);
-    const bool seg_end = pair_end || (cc.u + nb == u1);
-    if (seg_end) {
-      // ---- merge the NWK warps' partial softmax states of this segment ----
-      float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-      la += __shfl_xor_sync(0xffffffffu, la, 2);
-      float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-      if ((lane & 3) == 0) {
-        if (rA < G) { mrg_ml[(wk * G + rA) * 2] = m0; mrg_ml[(wk * G + rA) * 2 + 1] = la; }
-        if (rB < G) { mrg_ml[(wk * G + rB) * 2] = m1; mrg_ml[(wk * G + rB) * 2 + 1] = lb; }
-      }
-#pragma unroll
-      for (int n8 = 0; n8 < D / 8; ++n8) {
-        const int col = n8 * 8 + (lane & 3) * 2;
-        if (rA < G) {
-          mrg_o[(wk * G + rA) * D + col] = o[n8][0];
-          mrg_o[(wk * G + rA) * D + col + 1] = o[n8][1];
-        }
-        if (rB < G) {
-          mrg_o[(wk * G + rB) * D + col] = o[n8][2];
-          mrg_o[(wk * G + rB) * D + col + 1] = o[n8][3];
-        }
-      }
-      __syncthreads();
-      const bool complete = (seg_first_k == 0) && pair_end;
-      const int64_t pair = (int64_t)cc.b * Hkv + cc.hk;
-      const int64_t pslot_idx = pair + c;
-      __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)cc.hk * G) * D;
-      for (int idx = tid; idx < G * D; idx += C::kThreads) {
-        const int g = idx / D, d = idx - (idx / D) * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kNWK; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
-        float acc = 0.f, den = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNWK; ++w) {
-          const float mw = mrg_ml[(w * G + g) * 2];
-          const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-          acc += f * mrg_o[(w * G + g) * D + d];
-          den += f * mrg_ml[(w * G + g) * 2 + 1];
-        }
-        if (complete) {
-          outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
-        } else {
-          p.part_o[(pslot_idx * G + g) * D + d] = acc;
-          if (d == 0) p.part_ml[pslot_idx * G + g] = make_float2(M, den);
-        }
-      }
-      __syncthreads();
-      seg_start = true;
+    // ---- merge the key groups' partial softmax states of this segment ----
+    float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+    la += __shfl_xor_sync(0xffffffffu, la, 2);
+    float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+    if ((lane & 3) == 0) {
+      if (rA < G) { mrg_ml[(wk * G + rA) * 2] = m0; mrg_ml[(wk * G + rA) * 2 + 1] = la; }
+      if (rB < G) { mrg_ml[(wk * G + rB) * 2] = m1; mrg_ml[(wk * G + rB) * 2 + 1] = lb; }
     }
-    advance(cc, nb);
-    cslot = (cslot + 1) % STAGES;
+#pragma unroll
+    for (int n8 = 0; n8 < D / 8; ++n8) {
+      const int col = n8 * 8 + (lane & 3) * 2;
+      if (rA < G) *reinterpret_cast<float2*>(&mrg_o[(wk * G + rA) * D + col]) = make_float2(o[n8][0], o[n8][1]);
+      if (rB < G) *reinterpret_cast<float2*>(&mrg_o[(wk * G + rB) * D + col]) = make_float2(o[n8][2], o[n8][3]);
+    }
+    named_barrier(1, C::kConsumers * 32);
+    const bool complete = (first_k == 0) && (first_k + nb_seg == cc.nblk);
+    const int64_t pair = (int64_t)cc.b * Hkv + cc.hk;
+    const int64_t pslot = pair + c;
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)cc.hk * G) * D;
+    for (int idx = tid; idx < G * D; idx += C::kConsumers * 32) {
+      const int g = idx / D, d = idx - (idx / D) * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::kNWK; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
+      float acc = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::kNWK; ++w) {
+        const float mw = mrg_ml[(w * G + g) * 2];
+        const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+        acc += f * mrg_o[(w * G + g) * D + d];
+        den += f * mrg_ml[(w * G + g) * 2 + 1];
+      }
+      if (complete) {
+        outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+      } else {
+        p.part_o[(pslot * G + g) * D + d] = acc;
+        if (d == 0) p.part_ml[pslot * G + g] = make_float2(M, den);
+      }
+    }
+    named_barrier(1, C::kConsumers * 32);
+    i0 += nb_seg;
+    advance(cc, nb_seg);
   }
-  cp_async_wait<0>();
 }
 
 // Merge the partials of pairs that were cut across CTAs; zero-fill empty sequences.
@@ -432,20 +462,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   }
 }
 
-template <int D, int RT, int STAGES>
-size_t split_smem_bytes(int G, int B) {
-  using C = Cfg<D, RT, STAGES>;
-  return (size_t)STAGES * C::kStageBytes + (size_t)kNWK * G * (D + 2) * 4 + (size_t)(B + 1) * 4;
-}
-
-template <int D, int RT, int STAGES>
-cudaError_t launch_split(const DecodeParams& p, cudaStream_t s) {
-  using C = Cfg<D, RT, STAGES>;
-  const size_t smem = split_smem_bytes<D, RT, STAGES>(p.group, p.batch);
-  auto kern = decode_split_kernel<D, RT, STAGES>;
+template <int D, int RT>
+cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  using C = Cfg<D, RT>;
+  const size_t smem = split_smem_bytes<D, RT>(p.group, p.batch);
+  auto kern = decode_split_kernel<D, RT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.num_ctas, C::kThreads, smem, s>>>(p);
+  kern<<<p.num_ctas, C::kThreads, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -466,14 +490,27 @@ int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t ma
   return (int)n;
 }
 
+size_t decode_smem_bytes(int head_dim, int group, int batch) {
+  const int RT = group <= 16 ? 1 : 2;
+  if (head_dim == 128)
+    return RT == 1 ? split_smem_bytes<128, 1>(group, batch) : split_smem_bytes<128, 2>(group, batch);
+  return RT == 1 ? split_smem_bytes<64, 1>(group, batch) : split_smem_bytes<64, 2>(group, batch);
+}
+
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
   const int D = p.pool.head_dim;
   const int RT = p.group <= 16 ? 1 : 2;
+  const int R = p.pool.page_size < 16 ? p.pool.page_size : 16;
+  const int64_t rows = p.pool.num_pages * (int64_t)p.pool.page_size;
+  CUtensorMap tk, tv;
+  if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R) ||
+      !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   if (D == 128) {
-    e = RT == 1 ? launch_split<128, 1, 4>(p, s) : launch_split<128, 2, 4>(p, s);
+    e = RT == 1 ? launch_split<128, 1>(p, tk, tv, s) : launch_split<128, 2>(p, tk, tv, s);
   } else {
-    e = RT == 1 ? launch_split<64, 1, 8>(p, s) : launch_split<64, 2, 8>(p, s);
+    e = RT == 1 ? launch_split<64, 1>(p, tk, tv, s) : launch_split<64, 2>(p, tk, tv, s);
   }
   if (e != cudaSuccess) return e;
   const int pairs = p.batch * p.pool.num_kv_heads;

@@ -1,6 +1,7 @@
 // Launch-side declarations shared between the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,6 +54,13 @@ int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ct
 int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
                     int32_t head_dim, int32_t group);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
+// Dynamic shared memory the bf16 decode split kernel needs.
+size_t decode_smem_bytes(int head_dim, int group, int batch);
+
+// TMA descriptor of a bf16 pool viewed as {head_dim, num_kv_heads, rows}, box
+// {64, 1, box_rows}, 128-byte swizzle.  False if the driver refuses it.
+bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
+                      int box_rows);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {

@@ -77,6 +77,7 @@ def test_decode_validation(L):
     assert _decode(L, _pool(), hq=12) == capi.PA_ERR_SHAPE          # 12 % 8 != 0
     assert _decode(L, _pool(d=96)) == capi.PA_ERR_UNSUPPORTED       # bf16 head_dim
     assert _decode(L, _pool(ps=12), msl=40) == capi.PA_ERR_UNSUPPORTED  # bf16 page_size
+    assert _decode(L, _pool(ps=4), msl=16) == capi.PA_ERR_UNSUPPORTED   # bf16 decode: page_size >= 8
     assert _decode(L, _pool(hkv=1), hq=64) == capi.PA_ERR_UNSUPPORTED  # group 64
     assert _decode(L, _pool(), scale=float("nan")) == capi.PA_ERR_RANGE
     assert _decode(L, _pool(), msl=65) == capi.PA_ERR_SHAPE          # > max_blocks * page_size
