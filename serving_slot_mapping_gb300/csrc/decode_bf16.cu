@@ -12,11 +12,13 @@
 //   list is cut into `num_ctas` equal contiguous ranges (one persistent CTA
 //   per SM).  Every CTA streams the same number of KV bytes whatever the mix
 //   of context lengths, so there is no tail of idle SMs.
-// * Inside a CTA one producer warp walks the range and, for each block,
+// * Inside a CTA a producer warp walks the range and, for each block,
 //   follows block_table to the page and issues TMA tensor copies of the K and
 //   V rows of that KV head into a ring of mbarrier-guarded stages (128 KB of
-//   KV in flight per SM).  Per pair ("segment") it also bulk-copies the G
-//   query rows that share the KV head.
+//   KV in flight per SM).  The ring is split among the consumer key groups;
+//   each slot has one issuing lane and one consuming group, both in order,
+//   and the lanes issue concurrently.  A second producer warp bulk-copies,
+//   per pair ("segment"), the G query rows that share the KV head.
 // * Consumer warps (key groups x row tiles of 16 query heads) take blocks
 //   round-robin: S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
 //   fp32 accumulate), online softmax in the log2 domain, output rescale
@@ -73,12 +75,13 @@ template <int D, int RT>
 struct Cfg {
   static constexpr int kNWK = RT == 1 ? 8 : 4;            // key groups
   static constexpr int kConsumers = kNWK * RT;            // consumer warps
-  static constexpr int kThreads = 32 * (kConsumers + 1);  // + one producer warp
+  static constexpr int kThreads = 32 * (kConsumers + 2);  // + KV producer warp + Q producer warp
   static constexpr int kSlabs = D / 64;                   // 128-byte swizzle slabs per row
   static constexpr int kSlabBytes = 16 * 128;             // one slab of a 16-key tile
   static constexpr int kTileBytes = kSlabs * kSlabBytes;  // one 16-key K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kStages = D == 128 ? 16 : 32;      // 128 KB of KV in flight per SM
+  static constexpr int kSPG = kStages / kNWK;             // ring slots owned by one key group
   static constexpr int kQRows = 16 * RT;
   static constexpr int kQSlotBytes = kQRows * D * 2;
   static constexpr int kRingBytes = kStages * kStageBytes;
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
   auto qempty_bar = [&](int s) { return bars + 8u * (2 * S + 2 + s); };
   float* mrg_o = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [NWK][G][D]
   float* mrg_ml = mrg_o + C::kNWK * G * D;                           // [NWK][G][2]
-  int* prefix = reinterpret_cast<int*>(mrg_ml + C::kNWK * G * 2);    // [B+1]
+  int* prefix = reinterpret_cast<int*>(mrg_ml + C::kNWK * G * 2);    // [B+1] 16-key blocks before b
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
@@ -197,52 +200,77 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
 
   const __nv_bfloat16* qglob = static_cast<const __nv_bfloat16*>(p.q);
 
-  if (warp == C::kConsumers) {
-    // ======================= producer warp =======================
+  if (warp == C::kConsumers + 1) {
+    // ======================= Q producer =======================
+    // Walks the CTA's segments (pairs) in order and bulk-copies each pair's
+    // G query rows into a 2-slot ring; in-order issue keeps every parity wait
+    // at most one phase ahead of the barrier.
     if (lane != 0) return;
-    const int R = ps < 16 ? ps : 16;  // rows per TMA box (page_size >= 8)
-    Cursor pc = locate(u0);
-    int seg = -1;
+    Cursor cur = locate(u0);
     bool alive = true;
-    for (int64_t i = 0; pc.u < u1; ++i) {
-      if (i == 0 || pc.k == 0) {  // a segment (pair) starts: stage its G query rows
-        ++seg;
-        const int qs = seg & 1;
-        if (seg >= 2 && alive) alive = mbar_wait(qempty_bar(qs), ((seg >> 1) - 1) & 1, p.err);
-        const uint32_t qbytes = (uint32_t)(G * D * 2);
-        mbar_arrive_expect_tx(qfull_bar(qs), qbytes);
-        bulk_load(smem_u32(qring + qs * C::kQSlotBytes),
-                  qglob + ((int64_t)pc.b * Hq + (int64_t)pc.hk * G) * D, qbytes, qfull_bar(qs));
-      }
-      const int slot = (int)(i % S);
-      if (i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
-      const int key0 = pc.k * 16;
-      const int32_t* bt = p.block_table + (int64_t)pc.b * p.max_blocks;
-      int rows[2] = {-1, -1};
-      int nbox = 0;
-      for (int t = 0; t < 16 / R; ++t) {
-        const int kk = key0 + t * R;
-        if (kk >= pc.L) break;
-        const int page = __ldg(bt + (kk >> pshift));
-        if (page < 0 || page >= p.pool.num_pages) {
-          record_error(p.err, ERR_BLOCK_TABLE, page);
-          continue;
+    for (int seg = 0; cur.u < u1; ++seg) {
+      const int qs = seg & 1;
+      if (seg >= 2 && alive) alive = mbar_wait(qempty_bar(qs), ((seg >> 1) - 1) & 1, p.err);
+      const uint32_t qbytes = (uint32_t)(G * D * 2);
+      mbar_arrive_expect_tx(qfull_bar(qs), qbytes);
+      bulk_load(smem_u32(qring + qs * C::kQSlotBytes), qglob + ((int64_t)cur.b * Hq + (int64_t)cur.hk * G) * D,
+                qbytes, qfull_bar(qs));
+      advance(cur, (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u));
+    }
+    return;
+  }
+
+  if (warp == C::kConsumers) {
+    // ======================= KV producer =======================
+    // Ring slot l belongs to key group g = l / kSPG, which consumes its blocks
+    // in order; lane l issues that group's blocks t = r, r + kSPG, ... (r =
+    // l % kSPG), so each slot has one in-order writer and one in-order reader.
+    // The lanes issue concurrently: measured on GB300, one thread issuing 2 KB
+    // TMA boxes back to back streams only ~2.6 TB/s, sixteen lanes ~5.5 TB/s.
+    if (lane >= S) return;
+    const int g = lane / C::kSPG, r = lane % C::kSPG;
+    const int slot = lane;
+    const int R = ps < 16 ? ps : 16;  // rows per TMA box (page_size >= 8)
+    Cursor cur = locate(u0);
+    int64_t tcount = 0;  // blocks of group g before the current segment
+    bool alive = true;
+    while (cur.u < u1) {
+      const int nb_seg = (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u);
+      const int cnt = nb_seg > g ? (nb_seg - g + C::kNWK - 1) / C::kNWK : 0;
+      int64_t t = tcount + (((r - tcount) % C::kSPG) + C::kSPG) % C::kSPG;  // first t >= tcount, t % kSPG == r
+      const int32_t* bt = p.block_table + (int64_t)cur.b * p.max_blocks;
+      for (; t < tcount + cnt; t += C::kSPG) {
+        const int j = g + (int)(t - tcount) * C::kNWK;  // block within the segment
+        if (t >= C::kSPG && alive)
+          alive = mbar_wait(empty_bar(slot), (uint32_t)(((t / C::kSPG) - 1) & 1), p.err);
+        const int key0 = (cur.k + j) * 16;
+        int rows[2] = {-1, -1};
+        int nbox = 0;
+        for (int q = 0; q < 16 / R; ++q) {
+          const int kk = key0 + q * R;
+          if (kk >= cur.L) break;
+          const int page = __ldg(bt + (kk >> pshift));
+          if (page < 0 || page >= p.pool.num_pages) {
+            record_error(p.err, ERR_BLOCK_TABLE, page);
+            continue;
+          }
+          rows[q] = page * ps + (kk & (ps - 1));
+          ++nbox;
         }
-        rows[t] = page * ps + (kk & (ps - 1));
-        ++nbox;
-      }
-      mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(nbox * 2 * C::kSlabs * R * 128));
-      const uint32_t kdst = smem_u32(ring + slot * C::kStageBytes);
-      const uint32_t vdst = kdst + C::kTileBytes;
-      for (int t = 0; t < 16 / R; ++t) {
-        if (rows[t] < 0) continue;
+        mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(nbox * 2 * C::kSlabs * R * 128));
+        const uint32_t kdst = smem_u32(ring + slot * C::kStageBytes);
+        const uint32_t vdst = kdst + C::kTileBytes;
+        for (int q = 0; q < 16 / R; ++q) {
+          if (rows[q] < 0) continue;
 #pragma unroll
-        for (int sl = 0; sl < C::kSlabs; ++sl) {
-          tma_load_3d(kdst + sl * C::kSlabBytes + t * R * 128, &tmap_k, sl * 64, pc.hk, rows[t], full_bar(slot));
-          tma_load_3d(vdst + sl * C::kSlabBytes + t * R * 128, &tmap_v, sl * 64, pc.hk, rows[t], full_bar(slot));
+          for (int sl = 0; sl < C::kSlabs; ++sl) {
+            tma_load_3d(kdst + sl * C::kSlabBytes + q * R * 128, &tmap_k, sl * 64, cur.hk, rows[q], full_bar(slot));
+            tma_load_3d(vdst + sl * C::kSlabBytes + q * R * 128, &tmap_v, sl * 64, cur.hk, rows[q], full_bar(slot));
+          }
         }
       }
-      advance(pc, 1);
+      tcount += cnt;
+      advance(cur, nb_seg);
     }
     return;
   }
@@ -255,7 +283,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
   const int mi = lane >> 3, rr = lane & 7;
   Cursor cc = locate(u0);
   int seg = -1;
-  int64_t i0 = 0;  // stage index of the segment's first block
+  int64_t tg = 0;  // blocks this key group has consumed so far
   bool alive = true;
   while (cc.u < u1) {
     ++seg;
@@ -283,10 +311,9 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     for (int n8 = 0; n8 < D / 8; ++n8) o[n8][0] = o[n8][1] = o[n8][2] = o[n8][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int j = wk; j < nb_seg; j += C::kNWK) {
-      const int64_t stage = i0 + j;
-      const int slot = (int)(stage % S);
-      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((stage / S) & 1), p.err);
+    for (int j = wk; j < nb_seg; j += C::kNWK, ++tg) {
+      const int slot = wk * C::kSPG + (int)(tg % C::kSPG);
+      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((tg / C::kSPG) & 1), p.err);
       unsigned char* kt = ring + slot * C::kStageBytes;
       unsigned char* vt = kt + C::kTileBytes;
       const int valid = cc.L - (first_k + j) * 16;  // >= 1
@@ -403,7 +430,6 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
       }
     }
     named_barrier(1, C::kConsumers * 32);
-    i0 += nb_seg;
     advance(cc, nb_seg);
   }
 }
