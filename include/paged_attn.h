@@ -118,8 +118,11 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  * workspace     device scratch of at least
  *               paged_attention_decode_workspace_size(...) bytes (may be NULL
  *               when that size is 0), 16-byte aligned, owned by the caller and
- *               not shared by calls in flight at the same time.
- * bf16 path: head_dim in {64, 128}, page_size a power of two;
+ *               not shared by calls in flight at the same time.  Every call
+ *               clears the workspace's arrival counters (cudaMemsetAsync on
+ *               `stream`) before its kernel; no other part needs zeroing.
+ * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
+ * query heads per KV head, q 16-byte aligned;
  * f32 path: head_dim <= 256, any page_size.
  */
 size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
@@ -149,7 +152,8 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
  *   any stream capture on the device.
  * - All calls share the one array, which keeps the last call's contents;
  *   calls whose kernels overlap on the GPU (different streams, or unordered
- *   host threads) race on it.  Nothing in it needs to start zeroed.
+ *   host threads) race on it.  The part that must start zeroed is cleared
+ *   by every call.
  * - bf16 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
  *   workspace anyway).  A call whose partials would not fit, i.e. when
  *   paged_attention_decode_workspace_size(...) exceeds
