@@ -111,8 +111,7 @@ size_t decode_ws_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int ct
   if (batch <= 0 || hq <= 0 || hkv <= 0 || d <= 0) return 0;
   const int64_t slots = pa::decode_partial_slots(batch, hkv, ctas);
   const int64_t g = hq / hkv;
-  return align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256) +
-         align_up((size_t)batch * hkv * 4, 256);
+  return align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256);
 }
 
 }  // namespace
@@ -219,11 +218,7 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
   p.seq_lens = seq_lens;
   p.part_o = static_cast<float*>(workspace);
   const size_t o_bytes = align_up((size_t)(slots * group * pool->head_dim * 4), 256);
-  const size_t ml_bytes = align_up((size_t)(slots * group * 8), 256);
   p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
-  p.arrivals = reinterpret_cast<int*>(static_cast<char*>(workspace) + o_bytes + ml_bytes);
-  // The arrival counters must start at zero; clearing them is part of every call.
-  if (cudaMemsetAsync(p.arrivals, 0, (size_t)batch * pool->num_kv_heads * 4, s) != cudaSuccess) return PA_ERR_CUDA;
   p.batch = batch;
   p.num_q_heads = num_q_heads;
   p.group = group;

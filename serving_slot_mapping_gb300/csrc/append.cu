@@ -14,6 +14,9 @@ namespace pa {
 
 template <typename V>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  // The attention kernel that follows may start its prologue now; it waits
+  // (griddepcontrol.wait) for this grid before reading the pool.
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int64_t nvec = p.row_bytes / (int64_t)sizeof(V);

@@ -85,6 +85,33 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk, int row_bytes) {
   return row * row_bytes + ((chunk ^ (row & 7)) << 4);
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the grids this
+// one depends on have completed and their memory is visible (a no-op when
+// the kernel was not launched as a programmatic dependent);
+// griddep_launch_dependents lets the next kernel on the stream start its
+// prologue early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Launch with programmatic stream serialization allowed (see griddep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 __host__ __device__ __forceinline__ int ilog2_pow2(int x) {
   int r = 0;
   while ((1 << r) < x) ++r;

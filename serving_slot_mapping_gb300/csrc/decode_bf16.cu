@@ -1,5 +1,5 @@
 // paged_attention_decode, bf16 path: split-KV online-softmax decode over the
-// page pool, with the split combine fused in.
+// page pool plus a combine kernel, chained by programmatic dependent launch.
 //
 // What is computed (onnxruntime/mobius PR #395 "Add paged / block-table KV
 // cache export", "How it works": Gather(pool, block_table) then Attention
@@ -29,10 +29,13 @@
 // * At a segment end the key groups merge in shared memory.  A segment that
 //   covers a whole pair writes the bf16 output directly; a pair cut by a
 //   range boundary leaves one fp32 partial (m, l, o) per CTA in the
-//   workspace and counts itself on an arrival counter; the CTA that
-//   completes the count merges the partials with
-//   o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.  (A separate combine
-//   launch measured ~15 us of pure latency per call at batch 32.)
+//   workspace, and the combine kernel merges them with
+//   o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// * Both kernels are launched with programmatic stream serialization: the
+//   split kernel's prologue (barriers, the seq_len prefix, block-table reads)
+//   runs while the preceding append kernel finishes, and the combine kernel's
+//   launch and prologue overlap the split kernel's tail.  Every access to data
+//   an earlier kernel may write comes after griddepcontrol.wait.
 #include <math.h>
 
 #include "common.cuh"
@@ -123,7 +126,6 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
   float* mrg_ml = mrg_o + C::kNWK * G * D;                           // [NWK][G][2]
   int* prefix = reinterpret_cast<int*>(mrg_ml + C::kNWK * G * 2);    // [B+1] 16-key blocks before b
 
-  __shared__ int s_merge[3];  // last-arriver flag, first and last CTA of the pair
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
   const int max_len = p.max_blocks * ps;
@@ -166,11 +168,14 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
   const int64_t U = NB * Hkv;
   const int n = p.num_ctas, c = blockIdx.x;
   const int64_t u0 = (int64_t)c * U / n, u1 = (int64_t)(c + 1) * U / n;
+  griddep_launch_dependents();
+  if (warp < C::kConsumers) griddep_wait();  // before any output write
   // sequences with no key (seq_len 0) get out = 0; CTA b % n writes them
   for (int b = c; b < B; b += n) {
     if (prefix[b + 1] != prefix[b]) continue;
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (int64_t)b * Hq * D;
-    for (int idx = tid; idx < Hq * D; idx += C::kThreads) ob[idx] = __float2bfloat16_rn(0.f);
+    if (warp < C::kConsumers)
+      for (int idx = tid; idx < Hq * D; idx += C::kConsumers * 32) ob[idx] = __float2bfloat16_rn(0.f);
   }
   if (u0 >= u1) return;
 
@@ -217,6 +222,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     if (lane != 0) return;
     Cursor cur = locate(u0);
     bool alive = true;
+    griddep_wait();
     for (int seg = 0; cur.u < u1; ++seg) {
       const int qs = seg & 1;
       if (seg >= 2 && alive) alive = mbar_wait(qempty_bar(qs), ((seg >> 1) - 1) & 1, p.err);
@@ -243,6 +249,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     Cursor cur = locate(u0);
     int64_t tcount = 0;  // blocks of group g before the current segment
     bool alive = true;
+    griddep_wait();
     while (cur.u < u1) {
       const int nb_seg = (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u);
       const int cnt = nb_seg > g ? (nb_seg - g + C::kNWK - 1) / C::kNWK : 0;
@@ -438,48 +445,62 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
         if (d == 0) p.part_ml[pslot * G + g] = make_float2(M, den);
       }
     }
-    if (!complete) {
-      // The CTA whose partial completes this pair merges all of them:
-      // o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i over the CTAs i that
-      // cover the pair (writers fence, then count; the last one reads).
-      __threadfence();
-      named_barrier(1, C::kConsumers * 32);
-      if (tid == 0) {
-        const int64_t us = (int64_t)Hkv * prefix[cc.b] + (int64_t)cc.hk * cc.nblk;
-        const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(us + cc.nblk - 1, U, n);
-        int parts = 0;
-        for (int q = c0; q <= c1; ++q) parts += cta_range_empty(q, U, n) ? 0 : 1;
-        __threadfence();
-        const int prev = atomicAdd(p.arrivals + pair, 1);
-        __threadfence();
-        s_merge[0] = (prev + 1 == parts) ? 1 : 0;
-        s_merge[1] = c0;
-        s_merge[2] = c1;
-      }
-      named_barrier(1, C::kConsumers * 32);
-      if (s_merge[0]) {
-        const int c0 = s_merge[1], c1 = s_merge[2];
-        for (int idx = tid; idx < G * D; idx += C::kConsumers * 32) {
-          const int g = idx / D, d = idx - (idx / D) * D;
-          float M = -INFINITY;
-          for (int q = c0; q <= c1; ++q) {
-            if (cta_range_empty(q, U, n)) continue;
-            M = fmaxf(M, __ldcg(p.part_ml + (pair + q) * G + g).x);
-          }
-          float acc = 0.f, den = 0.f;
-          for (int q = c0; q <= c1; ++q) {
-            if (cta_range_empty(q, U, n)) continue;
-            const float2 ml = __ldcg(p.part_ml + (pair + q) * G + g);
-            const float f = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-            acc += f * __ldcg(p.part_o + ((pair + q) * G + g) * D + d);
-            den += f * ml.y;
-          }
-          outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
-        }
-      }
-    }
     named_barrier(1, C::kConsumers * 32);
     advance(cc, nb_seg);
+  }
+}
+
+// Merge the partials of pairs that were cut across CTAs.
+__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int D) {
+  const int Hkv = p.pool.num_kv_heads;
+  const int G = p.group;
+  const int pair = blockIdx.x;
+  const int b = pair / Hkv, hk = pair - (pair / Hkv) * Hkv;
+  const int max_len = p.max_blocks * p.pool.page_size;
+  // The prologue reads only seq_lens and overlaps the split kernel's tail;
+  // partials are read after the split grid has completed.
+  __shared__ long long red[2][4];
+  long long before = 0, total = 0;
+  for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+    const int nb = (seq_len_of(p.seq_lens, i, max_len) + 15) >> 4;
+    total += nb;
+    if (i < b) before += nb;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = before; red[1][threadIdx.x >> 5] = total; }
+  __syncthreads();
+  before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+  total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  const int nblk = (seq_len_of(p.seq_lens, b, max_len) + 15) >> 4;
+  __nv_bfloat16* outp =
+      static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
+  griddep_wait();
+  if (nblk == 0) return;  // zeroed by the split kernel
+  const int64_t U = total * Hkv;
+  const int64_t us = before * Hkv + (int64_t)hk * nblk, ue = us + nblk;
+  const int c0 = cta_of_unit(us, U, p.num_ctas), c1 = cta_of_unit(ue - 1, U, p.num_ctas);
+  if (c0 == c1) return;  // written by the split kernel
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, d = idx - (idx / D) * D;
+    float M = -INFINITY;
+    for (int cc = c0; cc <= c1; ++cc) {
+      if (cta_range_empty(cc, U, p.num_ctas)) continue;  // wrote no partial
+      M = fmaxf(M, p.part_ml[((int64_t)pair + cc) * G + g].x);
+    }
+    float acc = 0.f, den = 0.f;
+    for (int cc = c0; cc <= c1; ++cc) {
+      if (cta_range_empty(cc, U, p.num_ctas)) continue;
+      const int64_t sidx = (int64_t)pair + cc;
+      const float2 ml = p.part_ml[sidx * G + g];
+      const float f = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+      acc += f * p.part_o[(sidx * G + g) * D + d];
+      den += f * ml.y;
+    }
+    outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
   }
 }
 
@@ -490,8 +511,7 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUt
   auto kern = decode_split_kernel<D, RT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.num_ctas, C::kThreads, smem, s>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.num_ctas), dim3(C::kThreads), smem, s, tk, tv, p);
 }
 
 }  // namespace
@@ -533,7 +553,8 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
   } else {
     e = RT == 1 ? launch_split<64, 1>(p, tk, tv, s) : launch_split<64, 2>(p, tk, tv, s);
   }
-  return e;
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, D);
 }
 
 }  // namespace pa

@@ -41,7 +41,6 @@ struct DecodeParams {
   const int32_t* seq_lens;
   float* part_o;          // [slots, G, D] fp32 unnormalised partial outputs
   float2* part_ml;        // [slots, G] (running max in log2 units, denominator)
-  int* arrivals;          // [B * Hkv] partials written per cut pair; zero at launch
   int32_t batch;
   int32_t num_q_heads;
   int32_t group;          // G = Hq / Hkv
