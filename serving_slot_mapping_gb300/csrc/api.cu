@@ -107,9 +107,9 @@ constexpr double kLog2e = 1.4426950408889634;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t decode_ws_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int ctas) {
+size_t decode_ws_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int ctas, int hb) {
   if (batch <= 0 || hq <= 0 || hkv <= 0 || d <= 0) return 0;
-  const int64_t slots = pa::decode_partial_slots(batch, hkv, ctas);
+  const int64_t slots = pa::decode_partial_slots(batch, hkv, ctas, hb);
   const int64_t g = hq / hkv;
   return align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256);
 }
@@ -166,7 +166,10 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
 size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                              int32_t head_dim, int32_t dtype) {
   if (dtype != PA_DTYPE_BF16) return 0;
-  return decode_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_sms());
+  if (num_kv_heads <= 0 || num_q_heads <= 0) return 0;
+  // heads per box for page_size >= 16 is an upper bound for every page size
+  const int hb = pa::decode_heads_per_box(num_kv_heads, num_q_heads / num_kv_heads, 16);
+  return decode_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_sms(), hb);
 }
 
 pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
@@ -203,13 +206,14 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
   }
   if (pool->page_size < 8) return PA_ERR_UNSUPPORTED;  // TMA boxes of >= 8 rows
   if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
-  const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, pool->head_dim,
-                                       group);
-  const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas);
+  const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
+  const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, hb);
+  const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas, hb);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
-  if (pa::decode_smem_bytes(pool->head_dim, group, batch) > (size_t)max_smem_optin()) return PA_ERR_UNSUPPORTED;
-  const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas);
+  const int budget = max_smem_optin();
+  if (pa::decode_smem_bytes(pool->head_dim, group, batch, hb, budget) > (size_t)budget) return PA_ERR_UNSUPPORTED;
+  const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas, hb);
   pa::DecodeParams p;
   p.pool = g;
   p.q = q;
@@ -224,6 +228,8 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
   p.group = group;
   p.max_blocks = max_blocks_per_seq;
   p.num_ctas = ctas;
+  p.heads_per_box = hb;
+  p.smem_budget = budget;
   p.scale_log2 = (float)((double)scale * kLog2e);
   p.err = error_word();
   return pa::launch_decode_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -7,35 +7,36 @@
 //   out[b, h] = softmax_j(scale * q[b,h] . K_b[j, h/G]) V_b[j, h/G],  j < L_b
 //
 // Work decomposition (GB300-first, not from the pages):
-// * The unit of work is a 16-key block of one (sequence, KV head) pair.  All
-//   units of the batch are laid out in one list, sequence-major, and the
-//   list is cut into `num_ctas` equal contiguous ranges (one persistent CTA
-//   per SM).  Every CTA streams the same number of KV bytes whatever the mix
-//   of context lengths, so there is no tail of idle SMs.
-// * Inside a CTA a producer warp walks the range and, for each block,
-//   follows block_table to the page and issues TMA tensor copies of the K and
-//   V rows of that KV head into a ring of mbarrier-guarded stages (128 KB of
-//   KV in flight per SM).  The ring is split among the consumer key groups;
-//   each slot has one issuing lane and one consuming group, both in order,
-//   and the lanes issue concurrently.  A second producer warp bulk-copies,
-//   per pair ("segment"), the G query rows that share the KV head.
-// * Consumer warps (key groups x row tiles of 16 query heads) take blocks
-//   round-robin: S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
+// * The unit of work is one 16-key block of one sequence for a box of HB KV
+//   heads (HB = the largest power of two <= 8 dividing num_kv_heads; 1 for
+//   page_size 8).  All units are laid out sequence-major and cut into
+//   `num_ctas` equal contiguous ranges, one persistent CTA per SM, so every
+//   CTA streams the same number of KV bytes whatever the context-length mix.
+// * A producer warp follows block_table and loads each stage (NBS blocks x HB
+//   heads of K and V) with TMA tensor copies through a 3-D view of the pool
+//   {head_dim, slots, kv_heads}: one box {64, 16, HB} lands as HB tiles of
+//   16 rows x 128 B with the 128-byte swizzle.  For 8 KV heads a box is a
+//   16 KB slice of one page; measured on GB300, one thread issuing such boxes
+//   streams ~7.7 TB/s, while 2 KB boxes issued back to back by one thread
+//   reach only ~2.6 TB/s (boxes of small stages are issued by several lanes).
+//   A second producer warp bulk-copies, per segment, the query rows.
+// * Eight consumer warps map to (head in box, block in stage, row tile of 16
+//   query heads): S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
 //   fp32 accumulate), online softmax in the log2 domain, output rescale
 //   skipped when no running max moved.  Each page is read from HBM once for
-//   all G heads (GQA/MQA reuse).
-// * Keys at or past L_b are masked in S, and their V rows are zeroed in
-//   shared memory, so stale or NaN-poisoned slots never reach the output.
-// * At a segment end the key groups merge in shared memory.  A segment that
-//   covers a whole pair writes the bf16 output directly; a pair cut by a
-//   range boundary leaves one fp32 partial (m, l, o) per CTA in the
-//   workspace, and the combine kernel merges them with
+//   all G query heads of its KV head (GQA/MQA reuse).  Every consumer waits
+//   on every stage in order, so no mbarrier parity wait can run a phase ahead.
+// * Keys at or past L_b are masked in S and their V rows are zeroed in shared
+//   memory, so stale or NaN-poisoned slots never reach the output.
+// * At a segment (sequence x head box) end, warps that shared a head merge in
+//   shared memory; a segment covering the whole sequence writes bf16 output,
+//   a segment cut by a range boundary leaves one fp32 partial (m, l, o) per
+//   CTA, and the combine kernel merges them with
 //   o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
-// * Both kernels are launched with programmatic stream serialization: the
-//   split kernel's prologue (barriers, the seq_len prefix, block-table reads)
-//   runs while the preceding append kernel finishes, and the combine kernel's
-//   launch and prologue overlap the split kernel's tail.  Every access to data
-//   an earlier kernel may write comes after griddepcontrol.wait.
+// * Both kernels use programmatic stream serialization: the split kernel's
+//   prologue runs while the preceding append kernel finishes, and the combine
+//   kernel's launch overlaps the split kernel's tail.  Every access to data an
+//   earlier kernel may write comes after griddepcontrol.wait.
 #include <math.h>
 
 #include "common.cuh"
@@ -76,65 +77,77 @@ struct Cursor {
   int64_t u;
 };
 
-template <int D, int RT>
+// Compile-time shape of one configuration: HB heads per box, RT row tiles.
+template <int D, int HB, int RT>
 struct Cfg {
-  static constexpr int kNWK = RT == 1 ? 8 : 4;            // key groups
-  static constexpr int kConsumers = kNWK * RT;            // consumer warps
+  static constexpr int kConsumers = 8;
+  static constexpr int NBS = kConsumers / (HB * RT);      // blocks per stage
   static constexpr int kThreads = 32 * (kConsumers + 2);  // + KV producer warp + Q producer warp
   static constexpr int kSlabs = D / 64;                   // 128-byte swizzle slabs per row
-  static constexpr int kSlabBytes = 16 * 128;             // one slab of a 16-key tile
-  static constexpr int kTileBytes = kSlabs * kSlabBytes;  // one 16-key K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = D == 128 ? 16 : 32;      // 128 KB of KV in flight per SM
-  static constexpr int kSPG = kStages / kNWK;             // ring slots owned by one key group
-  static constexpr int kQRows = 16 * RT;
-  static constexpr int kQSlotBytes = kQRows * D * 2;
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarOffset = kRingBytes + 2 * kQSlotBytes;
-  static constexpr int kNumBars = 2 * kStages + 4;        // full[], empty[], qfull[2], qempty[2]
-  static constexpr int kMergeOffset = kBarOffset + kNumBars * 8;
+  static constexpr int kHeadTile = 16 * 128;              // one head, 16 rows, one slab
+  static constexpr int kBoxBytes = HB * kHeadTile;        // one {64, 16, HB} box
+  static constexpr int kTensorBytes = NBS * kSlabs * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kTensorBytes;    // K then V
 };
 
-template <int D, int RT>
-size_t split_smem_bytes(int G, int B) {
-  using C = Cfg<D, RT>;
-  return 1024 /* alignment slack */ + (size_t)C::kMergeOffset + (size_t)C::kNWK * G * (D + 2) * 4 +
-         (size_t)(B + 1) * 4;
+// Runtime shared-memory layout (stage count depends on G and B).
+struct Layout {
+  int stages, qslot, bar_off, mrg_off, prefix_off, total;
+};
+
+template <int D, int HB, int RT>
+__host__ __device__ inline Layout make_layout(int G, int B, int budget) {
+  using C = Cfg<D, HB, RT>;
+  Layout L;
+  L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
+  const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
+  const int fixed = 2 * L.qslot + (2 * 8 + 4) * 8 + merge + (B + 1) * 4 + 1024;
+  int s = (budget - fixed) / C::kStageBytes;
+  if (s > 8) s = 8;
+  L.stages = s;
+  L.bar_off = s * C::kStageBytes + 2 * L.qslot;
+  L.mrg_off = L.bar_off + (2 * s + 4) * 8;
+  L.prefix_off = L.mrg_off + merge;
+  L.total = L.prefix_off + (B + 1) * 4 + 1024;
+  return L;
 }
 
-template <int D, int RT>
-__global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
+template <int D, int HB, int RT>
+__global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         DecodeParams p) {
-  using C = Cfg<D, RT>;
-  constexpr int S = C::kStages;
+  using C = Cfg<D, HB, RT>;
+  constexpr int NBS = C::NBS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int G = p.group;
   const int B = p.batch;
   const int Hkv = p.pool.num_kv_heads;
+  const int Hg = Hkv / HB;  // head boxes per sequence
   const int Hq = p.num_q_heads;
+  const Layout lay = make_layout<D, HB, RT>(G, B, p.smem_budget);
+  const int S = lay.stages;
   unsigned char* ring = smem;
-  unsigned char* qring = smem + C::kRingBytes;
-  const uint32_t bars = smem_u32(smem + C::kBarOffset);
+  unsigned char* qring = smem + S * C::kStageBytes;
+  const uint32_t bars = smem_u32(smem + lay.bar_off);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto qfull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
   auto qempty_bar = [&](int s) { return bars + 8u * (2 * S + 2 + s); };
-  float* mrg_o = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [NWK][G][D]
-  float* mrg_ml = mrg_o + C::kNWK * G * D;                           // [NWK][G][2]
-  int* prefix = reinterpret_cast<int*>(mrg_ml + C::kNWK * G * 2);    // [B+1] 16-key blocks before b
+  float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [NBS][HB][G][D]
+  float* mrg_ml = mrg_o + NBS * HB * G * D;                           // [NBS][HB][G][2]
+  int* prefix = reinterpret_cast<int*>(smem + lay.prefix_off);        // [B+1] 16-key blocks before b
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
   const int max_len = p.max_blocks * ps;
 
-  // ---- set-up: barriers, zeroed Q slots (rows >= G stay zero), block prefix ----
+  // ---- set-up: barriers and the per-sequence block prefix (reads seq_lens only) ----
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), RT);
+      mbar_init(empty_bar(s), C::kConsumers);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(qfull_bar(s), 1);
@@ -142,11 +155,8 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     }
     fence_mbar_init();
   }
-  for (int i = tid; i < 2 * C::kQSlotBytes / 16; i += C::kThreads)
-    reinterpret_cast<uint4*>(qring)[i] = make_uint4(0, 0, 0, 0);
   for (int b = tid; b < B; b += C::kThreads) prefix[b + 1] = nblk_of(p.seq_lens, b, max_len, p.err);
   if (tid == 0) prefix[0] = 0;
-  fence_proxy_async_smem();
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
@@ -164,8 +174,9 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
   }
   __syncthreads();
 
+  // units: (b, head box hg, 16-key block k), sequence-major
   const int64_t NB = prefix[B];
-  const int64_t U = NB * Hkv;
+  const int64_t U = NB * Hg;
   const int n = p.num_ctas, c = blockIdx.x;
   const int64_t u0 = (int64_t)c * U / n, u1 = (int64_t)(c + 1) * U / n;
   griddep_launch_dependents();
@@ -181,7 +192,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
 
   auto locate = [&](int64_t u) {
     Cursor cur;
-    const int x = (int)(u / Hkv);
+    const int x = (int)(u / Hg);
     int lo = 0, hi = B;  // largest b in [0, B) with prefix[b] <= x
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -189,8 +200,8 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     }
     cur.b = lo;
     cur.nblk = prefix[lo + 1] - prefix[lo];
-    const int r = (int)(u - (int64_t)Hkv * prefix[lo]);
-    cur.hk = r / cur.nblk;
+    const int r = (int)(u - (int64_t)Hg * prefix[lo]);
+    cur.hk = r / cur.nblk;  // head box index
     cur.k = r - cur.hk * cur.nblk;
     cur.L = seq_len_of(p.seq_lens, cur.b, max_len);
     cur.u = u;
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     cur.k += nb;
     if (cur.k == cur.nblk) {
       cur.k = 0;
-      if (++cur.hk == Hkv) {
+      if (++cur.hk == Hg) {
         cur.hk = 0;
         do { ++cur.b; } while (cur.b < B && prefix[cur.b + 1] == prefix[cur.b]);
         if (cur.b < B) {
@@ -211,14 +222,20 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
       }
     }
   };
+  // blocks in the stage that starts at cur (a stage never crosses a segment)
+  auto stage_blocks = [&](const Cursor& cur) {
+    int64_t nb = cur.nblk - cur.k;
+    if (nb > NBS) nb = NBS;
+    if (nb > u1 - cur.u) nb = u1 - cur.u;
+    return (int)nb;
+  };
 
   const __nv_bfloat16* qglob = static_cast<const __nv_bfloat16*>(p.q);
 
   if (warp == C::kConsumers + 1) {
     // ======================= Q producer =======================
-    // Walks the CTA's segments (pairs) in order and bulk-copies each pair's
-    // G query rows into a 2-slot ring; in-order issue keeps every parity wait
-    // at most one phase ahead of the barrier.
+    // Segment by segment, in order, the HB*G query rows of the head box go to a
+    // 2-slot ring (in-order issue keeps each parity wait one phase ahead at most).
     if (lane != 0) return;
     Cursor cur = locate(u0);
     bool alive = true;
@@ -226,9 +243,9 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     for (int seg = 0; cur.u < u1; ++seg) {
       const int qs = seg & 1;
       if (seg >= 2 && alive) alive = mbar_wait(qempty_bar(qs), ((seg >> 1) - 1) & 1, p.err);
-      const uint32_t qbytes = (uint32_t)(G * D * 2);
+      const uint32_t qbytes = (uint32_t)(HB * G * D * 2);
       mbar_arrive_expect_tx(qfull_bar(qs), qbytes);
-      bulk_load(smem_u32(qring + qs * C::kQSlotBytes), qglob + ((int64_t)cur.b * Hq + (int64_t)cur.hk * G) * D,
+      bulk_load(smem_u32(qring + qs * lay.qslot), qglob + ((int64_t)cur.b * Hq + (int64_t)cur.hk * HB * G) * D,
                 qbytes, qfull_bar(qs));
       advance(cur, (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u));
     }
@@ -237,87 +254,83 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
 
   if (warp == C::kConsumers) {
     // ======================= KV producer =======================
-    // Ring slot l belongs to key group g = l / kSPG, which consumes its blocks
-    // in order; lane l issues that group's blocks t = r, r + kSPG, ... (r =
-    // l % kSPG), so each slot has one in-order writer and one in-order reader.
-    // The lanes issue concurrently: measured on GB300, one thread issuing 2 KB
-    // TMA boxes back to back streams only ~2.6 TB/s, sixteen lanes ~5.5 TB/s.
-    if (lane >= S) return;
-    const int g = lane / C::kSPG, r = lane % C::kSPG;
-    const int slot = lane;
-    const int R = ps < 16 ? ps : 16;  // rows per TMA box (page_size >= 8)
+    // One stage at a time: lane 0 claims the ring slot, then the lanes issue the
+    // stage's boxes (2 tensors x NBS blocks x slabs x 16/R) concurrently.
+    const int R = ps < 16 ? ps : 16;  // rows per box (page_size >= 8)
     Cursor cur = locate(u0);
-    int64_t tcount = 0;  // blocks of group g before the current segment
     bool alive = true;
     griddep_wait();
-    while (cur.u < u1) {
-      const int nb_seg = (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u);
-      const int cnt = nb_seg > g ? (nb_seg - g + C::kNWK - 1) / C::kNWK : 0;
-      int64_t t = tcount + (((r - tcount) % C::kSPG) + C::kSPG) % C::kSPG;  // first t >= tcount, t % kSPG == r
+    for (int64_t i = 0; cur.u < u1; ++i) {
+      const int nbs = stage_blocks(cur);
+      const int slot = (int)(i % S);
+      if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      const int boxes_per_block = 16 / R;
+      const int nops = 2 * nbs * C::kSlabs * boxes_per_block;
       const int32_t* bt = p.block_table + (int64_t)cur.b * p.max_blocks;
-      for (; t < tcount + cnt; t += C::kSPG) {
-        const int j = g + (int)(t - tcount) * C::kNWK;  // block within the segment
-        if (t >= C::kSPG && alive)
-          alive = mbar_wait(empty_bar(slot), (uint32_t)(((t / C::kSPG) - 1) & 1), p.err);
-        const int key0 = (cur.k + j) * 16;
-        int rows[2] = {-1, -1};
-        int nbox = 0;
-        for (int q = 0; q < 16 / R; ++q) {
-          const int kk = key0 + q * R;
-          if (kk >= cur.L) break;
-          const int page = __ldg(bt + (kk >> pshift));
-          if (page < 0 || page >= p.pool.num_pages) {
-            record_error(p.err, ERR_BLOCK_TABLE, page);
-            continue;
-          }
-          rows[q] = page * ps + (kk & (ps - 1));
-          ++nbox;
+      const uint32_t sbase = smem_u32(ring + slot * C::kStageBytes);
+      // op -> (tensor, block, slab, sub-box); -1 row = nothing to load
+      auto op_row = [&](int op, int& sl, int& jj, int& TT, int& q) {
+        q = op % boxes_per_block;
+        sl = (op / boxes_per_block) % C::kSlabs;
+        jj = (op / (boxes_per_block * C::kSlabs)) % nbs;
+        TT = op / (boxes_per_block * C::kSlabs * nbs);
+        const int kk = (cur.k + jj) * 16 + q * R;
+        if (kk >= cur.L) return -1;
+        const int page = __ldg(bt + (kk >> pshift));
+        if (page < 0 || page >= p.pool.num_pages) {
+          if (sl == 0 && TT == 0) record_error(p.err, ERR_BLOCK_TABLE, page);
+          return -1;
         }
-        mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(nbox * 2 * C::kSlabs * R * 128));
-        const uint32_t kdst = smem_u32(ring + slot * C::kStageBytes);
-        const uint32_t vdst = kdst + C::kTileBytes;
-        for (int q = 0; q < 16 / R; ++q) {
-          if (rows[q] < 0) continue;
-#pragma unroll
-          for (int sl = 0; sl < C::kSlabs; ++sl) {
-            tma_load_3d(kdst + sl * C::kSlabBytes + q * R * 128, &tmap_k, sl * 64, cur.hk, rows[q], full_bar(slot));
-            tma_load_3d(vdst + sl * C::kSlabBytes + q * R * 128, &tmap_v, sl * 64, cur.hk, rows[q], full_bar(slot));
-          }
-        }
+        return page * ps + (kk & (ps - 1));
+      };
+      int mine = 0;
+      for (int op = lane; op < nops; op += 32) {
+        int sl, jj, TT, q;
+        mine += op_row(op, sl, jj, TT, q) >= 0;
       }
-      tcount += cnt;
-      advance(cur, nb_seg);
+      const int issued = __reduce_add_sync(0xffffffffu, mine);
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB));
+      __syncwarp();
+      for (int op = lane; op < nops; op += 32) {
+        int sl, jj, TT, q;
+        const int row = op_row(op, sl, jj, TT, q);
+        if (row < 0) continue;
+        const uint32_t dst = sbase + (uint32_t)(((TT * NBS + jj) * C::kSlabs + sl) * C::kBoxBytes + q * R * 128);
+        tma_load_3d(dst, TT ? &tmap_v : &tmap_k, sl * 64, row, cur.hk * HB, full_bar(slot));
+      }
+      advance(cur, nbs);
     }
     return;
   }
 
   // ======================= consumer warps =======================
-  const int rt = warp / C::kNWK;  // row tile: query heads rt*16 .. rt*16+15 of the group
-  const int wk = warp % C::kNWK;  // key group: blocks j with j % kNWK == wk
+  const int h = warp % HB;               // head within the box
+  const int jw = (warp / HB) % NBS;      // block within each stage
+  const int rt = warp / (HB * NBS);      // row tile: query heads rt*16 .. rt*16+15 of the group
   const int rA = rt * 16 + (lane >> 2), rB = rA + 8;
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
   Cursor cc = locate(u0);
-  int seg = -1;
-  int64_t tg = 0;  // blocks this key group has consumed so far
+  int64_t i = 0;  // stage index
   bool alive = true;
-  while (cc.u < u1) {
-    ++seg;
-    const int nb_seg = (int)min((int64_t)(cc.nblk - cc.k), u1 - cc.u);
+  for (int seg = 0; cc.u < u1; ++seg) {
+    const int seg_blocks = (int)min((int64_t)(cc.nblk - cc.k), u1 - cc.u);
     const int first_k = cc.k;
-    // ---- the pair's query rows (A fragments of m16n8k16) ----
+    const int hk = cc.hk * HB + h;  // this warp's KV head
+    // ---- query rows of head hk (A fragments of m16n8k16; rows >= G are zero) ----
     uint32_t qf[D / 16][4];
     {
       const int qs = seg & 1;
       if (alive) alive = mbar_wait(qfull_bar(qs), (seg >> 1) & 1, p.err);
-      const uint32_t* qsm = reinterpret_cast<const uint32_t*>(qring + qs * C::kQSlotBytes);
+      const uint32_t* qsm = reinterpret_cast<const uint32_t*>(qring + qs * lay.qslot) + (h * G * D) / 2;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const int d0 = kk * 16 + (lane & 3) * 2;
-        qf[kk][0] = qsm[(rA * D + d0) >> 1];
-        qf[kk][1] = qsm[(rB * D + d0) >> 1];
-        qf[kk][2] = qsm[(rA * D + d0 + 8) >> 1];
-        qf[kk][3] = qsm[(rB * D + d0 + 8) >> 1];
+        qf[kk][0] = rA < G ? qsm[(rA * D + d0) >> 1] : 0u;
+        qf[kk][1] = rB < G ? qsm[(rB * D + d0) >> 1] : 0u;
+        qf[kk][2] = rA < G ? qsm[(rA * D + d0 + 8) >> 1] : 0u;
+        qf[kk][3] = rB < G ? qsm[(rB * D + d0 + 8) >> 1] : 0u;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty_bar(qs));
@@ -327,135 +340,170 @@ __global__ void __launch_bounds__(Cfg<D, RT>::kThreads, 1)
     for (int n8 = 0; n8 < D / 8; ++n8) o[n8][0] = o[n8][1] = o[n8][2] = o[n8][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int j = wk; j < nb_seg; j += C::kNWK, ++tg) {
-      const int slot = wk * C::kSPG + (int)(tg % C::kSPG);
-      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((tg / C::kSPG) & 1), p.err);
-      unsigned char* kt = ring + slot * C::kStageBytes;
-      unsigned char* vt = kt + C::kTileBytes;
-      const int valid = cc.L - (first_k + j) * 16;  // >= 1
-      if (valid < 16) {
-        // rows past L_b may hold stale or poisoned data: zero them in V (K is masked below)
-        for (int e = lane; e < (16 - valid) * C::kSlabs * 8; e += 32) {
-          const int row = valid + e / (C::kSlabs * 8);
-          const int rem = e % (C::kSlabs * 8);
-          *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::kSlabBytes + row * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+    for (int done = 0; done < seg_blocks; ++i) {
+      const int nbs = min(NBS, seg_blocks - done);
+      const int slot = (int)(i % S);
+      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((i / S) & 1), p.err);
+      if (jw < nbs) {
+        unsigned char* st = ring + slot * C::kStageBytes;
+        unsigned char* kt = st + (jw * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
+        unsigned char* vt = st + ((NBS + jw) * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
+        const int valid = cc.L - (first_k + done + jw) * 16;  // >= 1
+        if (valid < 16) {
+          // rows past L_b may hold stale or poisoned data: zero them in V (K is masked below)
+          for (int e = lane; e < (16 - valid) * C::kSlabs * 8; e += 32) {
+            const int row = valid + e / (C::kSlabs * 8);
+            const int rem = e % (C::kSlabs * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::kBoxBytes + row * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-      }
-      const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-      float s[2][4];
+        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+        float s[2][4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+        for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kSlabBytes), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qf[kk], b0, b1);
-        mma_bf16_16816(s[1], qf[kk], b2, b3);
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = t * 8 + (lane & 3) * 2 + (e & 1);
-          s[t][e] = key < valid ? s[t][e] * sl2 : -INFINITY;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kBoxBytes), b0, b1, b2, b3);
+          mma_bf16_16816(s[0], qf[kk], b0, b1);
+          mma_bf16_16816(s[1], qf[kk], b2, b3);
         }
-      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-      float p_[2][4];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        p_[t][0] = fast_exp2(s[t][0] - mn0);
-        p_[t][1] = fast_exp2(s[t][1] - mn0);
-        p_[t][2] = fast_exp2(s[t][2] - mn1);
-        p_[t][3] = fast_exp2(s[t][3] - mn1);
-      }
-      l0 = l0 * al0 + (p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1]);
-      l1 = l1 * al1 + (p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3]);
-      if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int n8 = 0; n8 < D / 8; ++n8) {
-          o[n8][0] *= al0; o[n8][1] *= al0;
-          o[n8][2] *= al1; o[n8][3] *= al1;
+          for (int e = 0; e < 4; ++e) {
+            const int key = t * 8 + (lane & 3) * 2 + (e & 1);
+            s[t][e] = key < valid ? s[t][e] * sl2 : -INFINITY;
+          }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+        float p_[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          p_[t][0] = fast_exp2(s[t][0] - mn0);
+          p_[t][1] = fast_exp2(s[t][1] - mn0);
+          p_[t][2] = fast_exp2(s[t][2] - mn1);
+          p_[t][3] = fast_exp2(s[t][3] - mn1);
         }
-      }
-      m0 = mn0;
-      m1 = mn1;
-      uint32_t pa[4];
-      pa[0] = pack_bf16(p_[0][0], p_[0][1]);
-      pa[1] = pack_bf16(p_[0][2], p_[0][3]);
-      pa[2] = pack_bf16(p_[1][0], p_[1][1]);
-      pa[3] = pack_bf16(p_[1][2], p_[1][3]);
+        l0 = l0 * al0 + (p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1]);
+        l1 = l1 * al1 + (p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3]);
+        if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
-      for (int jj = 0; jj < D / 16; ++jj) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kSlabBytes), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * jj], pa, b0, b1);
-        mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+          for (int n8 = 0; n8 < D / 8; ++n8) {
+            o[n8][0] *= al0; o[n8][1] *= al0;
+            o[n8][2] *= al1; o[n8][3] *= al1;
+          }
+        }
+        m0 = mn0;
+        m1 = mn1;
+        uint32_t pa[4];
+        pa[0] = pack_bf16(p_[0][0], p_[0][1]);
+        pa[1] = pack_bf16(p_[0][2], p_[0][3]);
+        pa[2] = pack_bf16(p_[1][0], p_[1][1]);
+        pa[3] = pack_bf16(p_[1][2], p_[1][3]);
+#pragma unroll
+        for (int jj = 0; jj < D / 16; ++jj) {
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kBoxBytes), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * jj], pa, b0, b1);
+          mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+        }
+        if (valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
       }
-      if (valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
+      done += nbs;
     }
 
-    // ---- merge the key groups' partial softmax states of this segment ----
+    // ---- segment end: normalise / merge / write ----
     float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
     la += __shfl_xor_sync(0xffffffffu, la, 2);
     float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
     lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-    if ((lane & 3) == 0) {
-      if (rA < G) { mrg_ml[(wk * G + rA) * 2] = m0; mrg_ml[(wk * G + rA) * 2 + 1] = la; }
-      if (rB < G) { mrg_ml[(wk * G + rB) * 2] = m1; mrg_ml[(wk * G + rB) * 2 + 1] = lb; }
-    }
+    const bool complete = (first_k == 0) && (seg_blocks == cc.nblk);
+    const int64_t seg_id = (int64_t)cc.b * Hg + cc.hk;
+    const int64_t pslot = (seg_id + c) * HB + h;  // unique per (segment, CTA, head)
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)hk * G) * D;
+    if (NBS == 1) {
+      // this warp holds its rows' whole segment state: write directly
+      const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
 #pragma unroll
-    for (int n8 = 0; n8 < D / 8; ++n8) {
-      const int col = n8 * 8 + (lane & 3) * 2;
-      if (rA < G) *reinterpret_cast<float2*>(&mrg_o[(wk * G + rA) * D + col]) = make_float2(o[n8][0], o[n8][1]);
-      if (rB < G) *reinterpret_cast<float2*>(&mrg_o[(wk * G + rB) * D + col]) = make_float2(o[n8][2], o[n8][3]);
-    }
-    named_barrier(1, C::kConsumers * 32);
-    const bool complete = (first_k == 0) && (first_k + nb_seg == cc.nblk);
-    const int64_t pair = (int64_t)cc.b * Hkv + cc.hk;
-    const int64_t pslot = pair + c;
-    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)cc.hk * G) * D;
-    for (int idx = tid; idx < G * D; idx += C::kConsumers * 32) {
-      const int g = idx / D, d = idx - (idx / D) * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < C::kNWK; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
-      float acc = 0.f, den = 0.f;
-#pragma unroll
-      for (int w = 0; w < C::kNWK; ++w) {
-        const float mw = mrg_ml[(w * G + g) * 2];
-        const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-        acc += f * mrg_o[(w * G + g) * D + d];
-        den += f * mrg_ml[(w * G + g) * 2 + 1];
+      for (int n8 = 0; n8 < D / 8; ++n8) {
+        const int col = n8 * 8 + (lane & 3) * 2;
+        if (complete) {
+          if (rA < G) *reinterpret_cast<uint32_t*>(outp + rA * D + col) = pack_bf16(o[n8][0] * ia, o[n8][1] * ia);
+          if (rB < G) *reinterpret_cast<uint32_t*>(outp + rB * D + col) = pack_bf16(o[n8][2] * ib, o[n8][3] * ib);
+        } else {
+          if (rA < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rA) * D + col) = make_float2(o[n8][0], o[n8][1]);
+          if (rB < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rB) * D + col) = make_float2(o[n8][2], o[n8][3]);
+        }
       }
-      if (complete) {
-        outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
-      } else {
-        p.part_o[(pslot * G + g) * D + d] = acc;
-        if (d == 0) p.part_ml[pslot * G + g] = make_float2(M, den);
+      if (!complete && (lane & 3) == 0) {
+        if (rA < G) p.part_ml[pslot * G + rA] = make_float2(m0, la);
+        if (rB < G) p.part_ml[pslot * G + rB] = make_float2(m1, lb);
       }
+    } else {
+      // NBS warps share each head: merge through shared memory
+      float* mo = mrg_o + ((jw * HB + h) * G) * D;
+      float* mml = mrg_ml + ((jw * HB + h) * G) * 2;
+      if ((lane & 3) == 0) {
+        if (rA < G) { mml[rA * 2] = m0; mml[rA * 2 + 1] = la; }
+        if (rB < G) { mml[rB * 2] = m1; mml[rB * 2 + 1] = lb; }
+      }
+#pragma unroll
+      for (int n8 = 0; n8 < D / 8; ++n8) {
+        const int col = n8 * 8 + (lane & 3) * 2;
+        if (rA < G) *reinterpret_cast<float2*>(&mo[rA * D + col]) = make_float2(o[n8][0], o[n8][1]);
+        if (rB < G) *reinterpret_cast<float2*>(&mo[rB * D + col]) = make_float2(o[n8][2], o[n8][3]);
+      }
+      named_barrier(1, C::kConsumers * 32);
+      for (int idx = tid; idx < HB * G * D; idx += C::kConsumers * 32) {
+        const int hh = idx / (G * D);
+        const int g = (idx / D) % G, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NBS; ++w) M = fmaxf(M, mrg_ml[((w * HB + hh) * G + g) * 2]);
+        float acc = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NBS; ++w) {
+          const float mw = mrg_ml[((w * HB + hh) * G + g) * 2];
+          const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+          acc += f * mrg_o[((w * HB + hh) * G + g) * D + d];
+          den += f * mrg_ml[((w * HB + hh) * G + g) * 2 + 1];
+        }
+        const int64_t hkk = (int64_t)cc.hk * HB + hh;
+        if (complete) {
+          static_cast<__nv_bfloat16*>(p.out)[((int64_t)cc.b * Hq + hkk * G + g) * D + d] =
+              __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+        } else {
+          const int64_t ps_ = (seg_id + c) * HB + hh;
+          p.part_o[(ps_ * G + g) * D + d] = acc;
+          if (d == 0) p.part_ml[ps_ * G + g] = make_float2(M, den);
+        }
+      }
+      named_barrier(1, C::kConsumers * 32);
     }
-    named_barrier(1, C::kConsumers * 32);
-    advance(cc, nb_seg);
+    advance(cc, seg_blocks);
   }
 }
 
-// Merge the partials of pairs that were cut across CTAs.
+// Merge the partials of (sequence, KV head) pairs that were cut across CTAs.
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int D) {
   const int Hkv = p.pool.num_kv_heads;
+  const int HB = p.heads_per_box;
+  const int Hg = Hkv / HB;
   const int G = p.group;
   const int pair = blockIdx.x;
   const int b = pair / Hkv, hk = pair - (pair / Hkv) * Hkv;
+  const int hg = hk / HB, h = hk - (hk / HB) * HB;
   const int max_len = p.max_blocks * p.pool.page_size;
   // The prologue reads only seq_lens and overlaps the split kernel's tail;
   // partials are read after the split grid has completed.
@@ -476,25 +524,26 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   const int nblk = (seq_len_of(p.seq_lens, b, max_len) + 15) >> 4;
-  __nv_bfloat16* outp =
-      static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
   griddep_wait();
   if (nblk == 0) return;  // zeroed by the split kernel
-  const int64_t U = total * Hkv;
-  const int64_t us = before * Hkv + (int64_t)hk * nblk, ue = us + nblk;
+  const int64_t U = total * Hg;
+  const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
   const int c0 = cta_of_unit(us, U, p.num_ctas), c1 = cta_of_unit(ue - 1, U, p.num_ctas);
   if (c0 == c1) return;  // written by the split kernel
+  const int64_t seg = (int64_t)b * Hg + hg;
+  __nv_bfloat16* outp =
+      static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D, d = idx - (idx / D) * D;
     float M = -INFINITY;
     for (int cc = c0; cc <= c1; ++cc) {
       if (cta_range_empty(cc, U, p.num_ctas)) continue;  // wrote no partial
-      M = fmaxf(M, p.part_ml[((int64_t)pair + cc) * G + g].x);
+      M = fmaxf(M, p.part_ml[((seg + cc) * HB + h) * G + g].x);
     }
     float acc = 0.f, den = 0.f;
     for (int cc = c0; cc <= c1; ++cc) {
       if (cta_range_empty(cc, U, p.num_ctas)) continue;
-      const int64_t sidx = (int64_t)pair + cc;
+      const int64_t sidx = (seg + cc) * HB + h;
       const float2 ml = p.part_ml[sidx * G + g];
       const float f = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
       acc += f * p.part_o[(sidx * G + g) * D + d];
@@ -504,38 +553,79 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   }
 }
 
-template <int D, int RT>
+template <int D, int HB, int RT>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-  using C = Cfg<D, RT>;
-  const size_t smem = split_smem_bytes<D, RT>(p.group, p.batch);
-  auto kern = decode_split_kernel<D, RT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  using C = Cfg<D, HB, RT>;
+  const Layout lay = make_layout<D, HB, RT>(p.group, p.batch, p.smem_budget);
+  if (lay.stages < 2) return cudaErrorInvalidConfiguration;
+  auto kern = decode_split_kernel<D, HB, RT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(p.num_ctas), dim3(C::kThreads), smem, s, tk, tv, p);
+  return launch_pdl(kern, dim3(p.num_ctas), dim3(C::kThreads), (size_t)lay.total, s, tk, tv, p);
+}
+
+template <int D>
+cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rt,
+                           cudaStream_t s) {
+  switch (p.heads_per_box * 10 + rt) {
+    case 81: return launch_split<D, 8, 1>(p, tk, tv, s);
+    case 41: return launch_split<D, 4, 1>(p, tk, tv, s);
+    case 21: return launch_split<D, 2, 1>(p, tk, tv, s);
+    case 11: return launch_split<D, 1, 1>(p, tk, tv, s);
+    case 42: return launch_split<D, 4, 2>(p, tk, tv, s);
+    case 22: return launch_split<D, 2, 2>(p, tk, tv, s);
+    case 12: return launch_split<D, 1, 2>(p, tk, tv, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas) {
-  return (int64_t)batch * num_kv_heads + num_ctas;
+int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size) {
+  const int rt = group <= 16 ? 1 : 2;
+  if (page_size < 16) return 1;
+  int hb = 1;
+  while (hb * 2 <= 8 / rt && num_kv_heads % (hb * 2) == 0) hb *= 2;
+  return hb;
 }
 
-int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
-                    int32_t head_dim, int32_t group) {
-  (void)head_dim;
-  (void)group;
-  const int64_t ubound = (int64_t)batch * num_kv_heads * (((int64_t)max_seq_len + 15) / 16);
+int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box) {
+  // (segment + CTA) * HB + head over segments (b, head box): B*Hkv + n*HB at most
+  return (int64_t)batch * num_kv_heads + (int64_t)num_ctas * heads_per_box;
+}
+
+int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t heads_per_box) {
+  const int64_t ubound = (int64_t)batch * (num_kv_heads / heads_per_box) * (((int64_t)max_seq_len + 15) / 16);
   int64_t n = num_sms;
   if (ubound < n) n = ubound;
   if (n < 1) n = 1;
   return (int)n;
 }
 
-size_t decode_smem_bytes(int head_dim, int group, int batch) {
-  const int RT = group <= 16 ? 1 : 2;
-  if (head_dim == 128)
-    return RT == 1 ? split_smem_bytes<128, 1>(group, batch) : split_smem_bytes<128, 2>(group, batch);
-  return RT == 1 ? split_smem_bytes<64, 1>(group, batch) : split_smem_bytes<64, 2>(group, batch);
+size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget) {
+  const int rt = group <= 16 ? 1 : 2;
+  Layout L;
+#define PA_LAYOUT(DD, HH, RR) L = make_layout<DD, HH, RR>(group, batch, budget)
+  const int key = (head_dim == 128 ? 1000 : 0) + heads_per_box * 10 + rt;
+  switch (key) {
+    case 1081: PA_LAYOUT(128, 8, 1); break;
+    case 1041: PA_LAYOUT(128, 4, 1); break;
+    case 1021: PA_LAYOUT(128, 2, 1); break;
+    case 1011: PA_LAYOUT(128, 1, 1); break;
+    case 1042: PA_LAYOUT(128, 4, 2); break;
+    case 1022: PA_LAYOUT(128, 2, 2); break;
+    case 1012: PA_LAYOUT(128, 1, 2); break;
+    case 81: PA_LAYOUT(64, 8, 1); break;
+    case 41: PA_LAYOUT(64, 4, 1); break;
+    case 21: PA_LAYOUT(64, 2, 1); break;
+    case 11: PA_LAYOUT(64, 1, 1); break;
+    case 42: PA_LAYOUT(64, 4, 2); break;
+    case 22: PA_LAYOUT(64, 2, 2); break;
+    case 12: PA_LAYOUT(64, 1, 2); break;
+    default: return (size_t)-1;
+  }
+#undef PA_LAYOUT
+  return L.stages >= 2 ? (size_t)L.total : (size_t)-1;
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
@@ -544,15 +634,10 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
   const int R = p.pool.page_size < 16 ? p.pool.page_size : 16;
   const int64_t rows = p.pool.num_pages * (int64_t)p.pool.page_size;
   CUtensorMap tk, tv;
-  if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R) ||
-      !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R))
+  if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box) ||
+      !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box))
     return cudaErrorInvalidValue;
-  cudaError_t e;
-  if (D == 128) {
-    e = RT == 1 ? launch_split<128, 1>(p, tk, tv, s) : launch_split<128, 2>(p, tk, tv, s);
-  } else {
-    e = RT == 1 ? launch_split<64, 1>(p, tk, tv, s) : launch_split<64, 2>(p, tk, tv, s);
-  }
+  cudaError_t e = D == 128 ? launch_split_d<128>(p, tk, tv, RT, s) : launch_split_d<64>(p, tk, tv, RT, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, D);
 }

@@ -41,6 +41,8 @@ struct DecodeParams {
   const int32_t* seq_lens;
   float* part_o;          // [slots, G, D] fp32 unnormalised partial outputs
   float2* part_ml;        // [slots, G] (running max in log2 units, denominator)
+  int32_t heads_per_box;  // HB: KV heads loaded per TMA box (power of two <= 8)
+  int32_t smem_budget;    // dynamic shared memory the stage ring is sized against
   int32_t batch;
   int32_t num_q_heads;
   int32_t group;          // G = Hq / Hkv
@@ -50,17 +52,20 @@ struct DecodeParams {
   unsigned long long* err;
 };
 // Number of partial slots the split kernel may write for this launch.
-int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas);
-int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
-                    int32_t head_dim, int32_t group);
+int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size);
+int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box);
+int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t heads_per_box);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 // Dynamic shared memory the bf16 decode split kernel needs.
-size_t decode_smem_bytes(int head_dim, int group, int batch);
+// (size_t)-1 when no stage ring of >= 2 stages fits the budget.
+size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget);
 
-// TMA descriptor of a bf16 pool viewed as {head_dim, num_kv_heads, rows}, box
-// {64, 1, box_rows}, 128-byte swizzle.  False if the driver refuses it.
+// TMA descriptor of a bf16 pool viewed as {head_dim, rows, num_kv_heads}
+// (strides num_kv_heads*head_dim*2 and head_dim*2 bytes), box {64, box_rows,
+// box_heads}, 128-byte swizzle: a box lands as box_heads tiles of box_rows x
+// 128 B.  False if the driver refuses it.
 bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
-                      int box_rows);
+                      int box_rows, int box_heads);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {
