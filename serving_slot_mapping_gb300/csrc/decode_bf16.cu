@@ -496,6 +496,11 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
 }
 
 // Merge the partials of (sequence, KV head) pairs that were cut across CTAs.
+// One CTA per pair; warp w merges rows g = w, w + 4, ... of the pair's G query
+// heads: lanes load the partials' (m, l) in parallel and reduce with
+// shuffles, then each lane accumulates 4 dims with float4 loads, all partials
+// in flight at once (a per-element loop over partials is a chain of dependent
+// loads: ~40 us at batch 32).
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int D) {
   const int Hkv = p.pool.num_kv_heads;
   const int HB = p.heads_per_box;
@@ -505,6 +510,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   const int b = pair / Hkv, hk = pair - (pair / Hkv) * Hkv;
   const int hg = hk / HB, h = hk - (hk / HB) * HB;
   const int max_len = p.max_blocks * p.pool.page_size;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // The prologue reads only seq_lens and overlaps the split kernel's tail;
   // partials are read after the split grid has completed.
   __shared__ long long red[2][4];
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
     before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
-  if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = before; red[1][threadIdx.x >> 5] = total; }
+  if (lane == 0) { red[0][warp] = before; red[1][warp] = total; }
   __syncthreads();
   before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
@@ -527,29 +533,50 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   griddep_wait();
   if (nblk == 0) return;  // zeroed by the split kernel
   const int64_t U = total * Hg;
+  const int n = p.num_ctas;
   const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
-  const int c0 = cta_of_unit(us, U, p.num_ctas), c1 = cta_of_unit(ue - 1, U, p.num_ctas);
+  const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(ue - 1, U, n);
   if (c0 == c1) return;  // written by the split kernel
+  const int nparts = c1 - c0 + 1;
+  const bool some_empty = U < n;  // only then can a CTA own no unit (and write no partial)
   const int64_t seg = (int64_t)b * Hg + hg;
   __nv_bfloat16* outp =
       static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D, d = idx - (idx / D) * D;
+  for (int g = warp; g < G; g += 4) {
+    // (m, l) of every partial: lanes stride over the parts
     float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) {
-      if (cta_range_empty(cc, U, p.num_ctas)) continue;  // wrote no partial
-      M = fmaxf(M, p.part_ml[((seg + cc) * HB + h) * G + g].x);
+    for (int q = lane; q < nparts; q += 32) {
+      if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
+      M = fmaxf(M, __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g).x);
     }
-    float acc = 0.f, den = 0.f;
-    for (int cc = c0; cc <= c1; ++cc) {
-      if (cta_range_empty(cc, U, p.num_ctas)) continue;
-      const int64_t sidx = (seg + cc) * HB + h;
-      const float2 ml = p.part_ml[sidx * G + g];
-      const float f = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-      acc += f * p.part_o[(sidx * G + g) * D + d];
-      den += f * ml.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    for (int q = lane; q < nparts; q += 32) {
+      if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
+      const float2 ml = __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
+      den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
     }
-    outp[idx] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    // weighted sum of the partial rows: lane owns dims 4*lane .. 4*lane+3 (D <= 128)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (4 * lane < D) {
+#pragma unroll 4
+      for (int q = 0; q < nparts; ++q) {
+        if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
+        const int64_t sidx = (seg + c0 + q) * HB + h;
+        const float mq = __ldcg(p.part_ml + sidx * G + g).x;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sidx * G + g) * D) + lane);
+        const float f = (mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
+        acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+      }
+      uint2 packed;
+      packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(outp + (int64_t)g * D + 4 * lane) = packed;
+    }
   }
 }
 
