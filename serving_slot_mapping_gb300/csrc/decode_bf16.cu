@@ -13,12 +13,12 @@
 //   `num_ctas` equal contiguous ranges, one persistent CTA per SM, so every
 //   CTA streams the same number of KV bytes whatever the context-length mix.
 // * A producer warp follows block_table and loads each stage (NBS blocks x HB
-//   heads of K and V) with TMA tensor copies through a 3-D view of the pool
-//   {head_dim, slots, kv_heads}: one box {64, 16, HB} lands as HB tiles of
-//   16 rows x 128 B with the 128-byte swizzle.  For 8 KV heads a box is a
-//   16 KB slice of one page; measured on GB300, one thread issuing such boxes
-//   streams ~7.7 TB/s, while 2 KB boxes issued back to back by one thread
-//   reach only ~2.6 TB/s (boxes of small stages are issued by several lanes).
+//   heads of K and V) with TMA tensor copies through a 4-D view of the pool
+//   {64 dims, slots, kv_heads, slabs}: one box {64, 16, HB, D/64} lands as
+//   HB tiles of 16 rows x 128 B per slab with the 128-byte swizzle.  For 8
+//   KV heads a box is a 32 KB slice of one page; measured on GB300, one
+//   thread issuing 16 KB boxes streams ~7.7 TB/s while 2 KB boxes issued back
+//   to back reach only ~2.6 TB/s, so ops are kept few and large.
 //   A second producer warp bulk-copies, per segment, the query rows.
 // * Eight consumer warps map to (head in box, block in stage, row tile of 16
 //   query heads): S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
   if (warp == C::kConsumers) {
     // ======================= KV producer =======================
     // One stage at a time: lane 0 claims the ring slot, then the lanes issue the
-    // stage's boxes (2 tensors x NBS blocks x slabs x 16/R) concurrently.
+    // stage's boxes concurrently.
     const int R = ps < 16 ? ps : 16;  // rows per box (page_size >= 8)
     Cursor cur = locate(u0);
     bool alive = true;
@@ -265,16 +265,20 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
       const int slot = (int)(i % S);
       if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      const int boxes_per_block = 16 / R;
-      const int nops = 2 * nbs * C::kSlabs * boxes_per_block;
+      // page_size >= 16: one box per (tensor, block) covers every slab; page_size
+      // 8: one box per (tensor, block, slab, 8-row half) so rows land at 16-row pitch
+      const int slabs_per_op = R == 16 ? C::kSlabs : 1;
+      const int boxes_per_block = (16 / R) * (C::kSlabs / slabs_per_op);
+      const int nops = 2 * nbs * boxes_per_block;
       const int32_t* bt = p.block_table + (int64_t)cur.b * p.max_blocks;
       const uint32_t sbase = smem_u32(ring + slot * C::kStageBytes);
       // op -> (tensor, block, slab, sub-box); -1 row = nothing to load
       auto op_row = [&](int op, int& sl, int& jj, int& TT, int& q) {
-        q = op % boxes_per_block;
-        sl = (op / boxes_per_block) % C::kSlabs;
-        jj = (op / (boxes_per_block * C::kSlabs)) % nbs;
-        TT = op / (boxes_per_block * C::kSlabs * nbs);
+        const int sub = op % boxes_per_block;
+        q = sub % (16 / R);
+        sl = sub / (16 / R);
+        jj = (op / boxes_per_block) % nbs;
+        TT = op / (boxes_per_block * nbs);
         const int kk = (cur.k + jj) * 16 + q * R;
         if (kk >= cur.L) return -1;
         const int page = __ldg(bt + (kk >> pshift));
@@ -290,14 +294,14 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         mine += op_row(op, sl, jj, TT, q) >= 0;
       }
       const int issued = __reduce_add_sync(0xffffffffu, mine);
-      if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB));
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB * slabs_per_op));
       __syncwarp();
       for (int op = lane; op < nops; op += 32) {
         int sl, jj, TT, q;
         const int row = op_row(op, sl, jj, TT, q);
         if (row < 0) continue;
         const uint32_t dst = sbase + (uint32_t)(((TT * NBS + jj) * C::kSlabs + sl) * C::kBoxBytes + q * R * 128);
-        tma_load_3d(dst, TT ? &tmap_v : &tmap_k, sl * 64, row, cur.hk * HB, full_bar(slot));
+        tma_load_4d(dst, TT ? &tmap_v : &tmap_k, 0, row, cur.hk * HB, sl, full_bar(slot));
       }
       advance(cur, nbs);
     }
@@ -661,8 +665,9 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
   const int R = p.pool.page_size < 16 ? p.pool.page_size : 16;
   const int64_t rows = p.pool.num_pages * (int64_t)p.pool.page_size;
   CUtensorMap tk, tv;
-  if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box) ||
-      !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box))
+  const int box_slabs = R == 16 ? D / 64 : 1;
+  if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs) ||
+      !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs))
     return cudaErrorInvalidValue;
   cudaError_t e = D == 128 ? launch_split_d<128>(p, tk, tv, RT, s) : launch_split_d<64>(p, tk, tv, RT, s);
   if (e != cudaSuccess) return e;

@@ -60,12 +60,12 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 // (size_t)-1 when no stage ring of >= 2 stages fits the budget.
 size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget);
 
-// TMA descriptor of a bf16 pool viewed as {head_dim, rows, num_kv_heads}
-// (strides num_kv_heads*head_dim*2 and head_dim*2 bytes), box {64, box_rows,
-// box_heads}, 128-byte swizzle: a box lands as box_heads tiles of box_rows x
-// 128 B.  False if the driver refuses it.
+// TMA descriptor of a bf16 pool viewed as {64, rows, num_kv_heads,
+// head_dim/64} (strides num_kv_heads*head_dim*2, head_dim*2 and 128 bytes),
+// box {64, box_rows, box_heads, box_slabs}, 128-byte swizzle: a box lands as
+// [slab][head][row][128 B].  False if the driver refuses it.
 bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
-                      int box_rows, int box_heads);
+                      int box_rows, int box_heads, int box_slabs);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {
