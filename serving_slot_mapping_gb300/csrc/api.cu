@@ -271,6 +271,7 @@ pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* o
     p.err = error_word();
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
+  if (batch > 65535 || pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y/z limits
   pa::PrefillParams p;
   p.pool = g;
   p.q = q;
