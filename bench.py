@@ -411,6 +411,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
 
     plan = rank_plan(args.workload, rank)
+    if plan.kind == "prefill":
+        return run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, bf16_sus, peak_src)
     rig = DecodeRig(plan, dev)
     g_step = capture(rig.step, stream)
     g_dec = capture(rig.decode, stream)
@@ -484,6 +486,48 @@ def run_ours(args, rank, world, local):
         "extra": extra,
     }
     return line
+
+
+def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, bf16_sus, peak_src):
+    """Main line for a prefill workload: append of the new tokens + varlen
+    causal prefill per step; value in TFLOP/s of visible (query, key) pairs."""
+    rig = PrefillRig(plan, dev)
+    g_step = capture(rig.step, stream)
+    g_pf = capture(rig.prefill, stream)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    times = timed_graph(g_step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    pf_times = timed_graph(g_pf, max(10, args.steps // 2), flush, stream)
+    clocks = sampler.stop()
+    ms_step = max_over_ranks(statistics.mean(times), world)
+    flops = wl.prefill_flops(plan)
+    value = sum_over_ranks(float(flops), world) / (ms_step * 1e-3) / 1e12
+    pf_ms = statistics.mean(pf_times)
+    achieved = flops / (pf_ms * 1e-3) / 1e12
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
+                   "num_kv_heads": plan.num_kv_heads, "head_dim": plan.head_dim,
+                   "page_size": plan.page_size, "new_tokens": plan.total_new,
+                   "visible_pairs": wl.prefill_visible_pairs(plan), "flops_per_step": flops,
+                   "step": "append new tokens + varlen causal prefill",
+                   "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16, 4), "traffic": traffic_for(f"prefill:{plan.name}"),
+                     "kernel": "paged_attention_prefill", "ms_per_launch": round(pf_ms, 5),
+                     "peak_source": peak_src, "peak_sustained": bf16_sus},
+        "clocks": clocks, "gpu_launches": 2 * args.steps,
+    }
 
 
 def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):

@@ -178,26 +178,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
       }
       if (j >= kNS && alive) alive = mbar_wait(bar(B_KVEMPTY + s), (uint32_t)(((j / kNS) - 1) & 1), p.err);
       unsigned char* st = kv_s + s * C::kStageBytes;
+      // thread lt copies 16-byte chunk (lt % kChunks) of rows r = lt / kChunks + kRowStep * i of
+      // both K and V: one block_table lookup per row, shared by the two tensors
+      constexpr int kRowStep = kLoadThreads / kChunks;
+      const int c = lt % kChunks;
 #pragma unroll 4
-      for (int idx = lt; idx < 2 * kBN * kChunks; idx += kLoadThreads) {
-        const int T = idx / (kBN * kChunks);
-        const int rem = idx - T * (kBN * kChunks);
-        const int r = rem / kChunks, c = rem % kChunks;
+      for (int r = lt / kChunks; r < kBN; r += kRowStep) {
         const int key = j * kBN + r;
-        bool ok = key < L;
-        const __nv_bfloat16* src = kpool;
-        if (ok) {
+        const uint32_t dst = smem_u32(st + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+        int64_t off = -1;
+        if (key < L) {
           const int page = __ldg(bt + (key >> pshift));
-          if (page < 0 || page >= p.pool.num_pages) {
-            record_error(p.err, ERR_BLOCK_TABLE, page);
-            ok = false;
-          } else {
-            src = (T ? vpool : kpool) + (((int64_t)page << pshift) + (key & (ps - 1))) * row_elems +
-                  (int64_t)hk * D + c * 8;
-          }
+          if (page < 0 || page >= p.pool.num_pages) record_error(p.err, ERR_BLOCK_TABLE, page);
+          else off = (((int64_t)page << pshift) + (key & (ps - 1))) * row_elems + (int64_t)hk * D + c * 8;
         }
-        cp_async_16(smem_u32(st + T * C::kKVTile + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src,
-                    ok ? 16 : 0);
+        cp_async_16(dst, off >= 0 ? kpool + off : kpool, off >= 0 ? 16 : 0);
+        cp_async_16(dst + C::kKVTile, off >= 0 ? vpool + off : vpool, off >= 0 ? 16 : 0);
       }
       cp_async_commit();
     }
