@@ -118,9 +118,9 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  * workspace     device scratch of at least
  *               paged_attention_decode_workspace_size(...) bytes (may be NULL
  *               when that size is 0), 16-byte aligned, owned by the caller and
- *               not shared by calls in flight at the same time.  Every call
- *               clears the workspace's arrival counters (cudaMemsetAsync on
- *               `stream`) before its kernel; no other part needs zeroing.
+ *               not shared by calls in flight at the same time.  Its
+ *               contents need no initialisation: each call writes every
+ *               partial it reads.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
  * query heads per KV head, q 16-byte aligned;
  * f32 path: head_dim <= 256, any page_size.
@@ -152,8 +152,7 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
  *   any stream capture on the device.
  * - All calls share the one array, which keeps the last call's contents;
  *   calls whose kernels overlap on the GPU (different streams, or unordered
- *   host threads) race on it.  The part that must start zeroed is cleared
- *   by every call.
+ *   host threads) race on it.  No part of it needs to start zeroed.
  * - bf16 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
  *   workspace anyway).  A call whose partials would not fit, i.e. when
  *   paged_attention_decode_workspace_size(...) exceeds
@@ -187,8 +186,9 @@ pa_status paged_attention_decode_static_scratch(const pa_kv_pool* pool, const vo
  *                  [batch] = total_q.
  * max_q_len        host upper bound of n_b (sizes the launch).
  * block_table, seq_lens, max_seq_len, scale: as for decode.
- * bf16 path: head_dim in {64, 128}, page_size a power of two;
- * f32 path: head_dim <= 256.
+ * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most
+ * 32 query heads per KV head;
+ * f32 path: head_dim <= 256, any page_size.
  */
 pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out,
                                   int32_t batch, int32_t num_q_heads,

@@ -94,7 +94,8 @@ pa_status check_attention(const pa_kv_pool* pool, int32_t batch, int32_t num_q_h
   if (!std::isfinite(scale)) return PA_ERR_RANGE;
   if (pool->dtype == PA_DTYPE_BF16) {
     if (pool->head_dim != 64 && pool->head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (!is_pow2(pool->page_size)) return PA_ERR_UNSUPPORTED;
+    // page-sized TMA boxes of 8-slot blocks
+    if (!is_pow2(pool->page_size) || pool->page_size < 8) return PA_ERR_UNSUPPORTED;
     if (num_q_heads / pool->num_kv_heads > 32) return PA_ERR_UNSUPPORTED;
     if (!aligned(pool->key_pool, 16) || !aligned(pool->value_pool, 16)) return PA_ERR_ALIGN;
   } else {
@@ -204,7 +205,6 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
     p.err = error_word();
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
-  if (pool->page_size < 8) return PA_ERR_UNSUPPORTED;  // TMA boxes of >= 8 rows
   if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
   const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
   const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, hb);

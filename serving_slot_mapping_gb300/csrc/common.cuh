@@ -75,7 +75,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32):
+// results below 2^-126 flush to zero, which changes no attention weight that
+// survives the bf16 / fp32 sums.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Swizzled byte offset of 16-byte chunk `chunk` of row `row` in a tile whose
 // rows are `row_bytes` long (row_bytes a multiple of 128): the chunk index is

@@ -15,10 +15,9 @@
 // per device with cudaGetSymbolAddress, with that device current, by the
 // first call on that device.  Every call shares the array: two calls whose
 // kernels overlap on the GPU (on different streams, or on one device from
-// several host threads without ordering) race on it.  The only part that
-// must start at zero, the per-pair arrival counters, is cleared by every call
-// (cudaMemsetAsync on the same stream, which allocates nothing); every
-// partial a call reads is written earlier in the same call.
+// several host threads without ordering) race on it.  Nothing in it needs to
+// start zeroed: every partial a call reads is written earlier in the same
+// call, by the split kernel that the combine kernel follows on the stream.
 #include <atomic>
 
 #include "../../include/paged_attn.h"

@@ -66,6 +66,13 @@ size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, 
 // [slab][head][row][128 B].  False if the driver refuses it.
 bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
                       int box_rows, int box_heads, int box_slabs);
+// The same pool as a 5-D tensor {64 dims, 8 slots, head_dim/64 slabs,
+// slots/8 blocks, heads}: one box {64, 8, head_dim/64, box_blocks, 1} lands as
+// [block][slab][8 slots][128 B] (128-byte swizzle), so 8-slot row groups sit at
+// a uniform stride of head_dim*16 bytes whatever the page size.  Needs
+// slots % 8 == 0.
+bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
+                              int box_blocks);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {

@@ -10,20 +10,24 @@
 // Tiling (GB300-first): a CTA owns 128 packed rows of one (sequence, KV head)
 // -- row r is query token r / G, query head hk*G + r % G -- so every K/V tile
 // in shared memory serves all G heads that read it.  Keys come in tiles of
-// 128 (eight 16-key pages).
-// * 4 loader warps stage Q once and K/V tiles (2-stage ring) with 16-byte
-//   cp.async through block_table into the 128-byte-swizzled UMMA layout;
-//   rows at or past L_b are zero-filled.  Pages are scattered, so a K tile's
-//   rows cannot come from one TMA box, and per-page boxes are too small to
-//   keep up with the tensor core.
-// * 1 MMA warp issues tcgen05.mma: S = Q K^T (M 128, N 128, fp32 in TMEM,
+// 128.
+// * 1 TMA warp stages K/V tiles (2-stage rings) page by page: its lanes look
+//   up one page each in block_table and issue one box per page (a whole
+//   128-key tile when pages hold >= 128 slots), so a tile costs 128 /
+//   min(page_size, 128) copies.  The 5-D view of the pool lands each box as
+//   [8-slot block][64-dim slab][8 slots][128 B], i.e. 8-key row groups at one
+//   uniform stride: exactly a K-major UMMA operand for K and an MN-major one
+//   for V.  Slots at or past L_b in the last tile are zeroed in V.
+// * 1 MMA thread issues tcgen05.mma: S = Q K^T (M 128, N 128, fp32 in TMEM,
 //   double-buffered so S(j+1) overlaps the softmax of S(j)) and O += P V
-//   (M 128, N head_dim, fp32 in TMEM), each committed to an mbarrier.
-// * 4 softmax warps own one TMEM lane (= one row) per thread: tcgen05.ld of S,
-//   causal mask, online softmax in the log2 domain with a lazily updated
-//   reference max (O and l are rescaled in TMEM only when the row max grows by
-//   more than 2^8), P written to shared memory as bf16 in the UMMA A layout,
-//   and at the end O / l written to global as bf16.
+//   (M 128, N head_dim, fp32 in TMEM), each committed to mbarriers.  It
+//   issues whichever of the next S and the next PV is ready first.
+// * 4 softmax warps own one TMEM lane (= one row) per thread: they stage their
+//   own Q row once (cp.async), then per key tile tcgen05.ld the row of S,
+//   apply the causal mask, run the online softmax in the log2 domain with a
+//   lazily updated reference max (O and l are rescaled in TMEM only when the
+//   row max grows by more than 2^8), write P to shared memory as bf16 in the
+//   UMMA A layout, and at the end write O / l to global as bf16.
 // Fully masked key tiles are never loaded or multiplied.
 #include <math.h>
 
@@ -41,40 +45,48 @@ constexpr int kBN = 128;             // keys per tile
 constexpr int kNS = 2;               // K/V ring stages
 constexpr int kSoftmaxWarps = 4;     // warps 0..3 (TMEM lane quarters 0..3)
 constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp0 = 5;        // warps 5..8
-constexpr int kLoadThreads = 128;
-constexpr int kThreads = 32 * 9;
-constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row tile (16 KB)
+constexpr int kTmaWarp = 5;
+// 6 warps: at most 2 per SM sub-partition, so each thread may hold 255
+// registers (the softmax keeps a whole 128-column row of S in registers)
+constexpr int kThreads = 32 * 6;
+constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row Q or P tile (16 KB)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 template <int D>
 struct PCfg {
   static constexpr int kSlabs = D / 64;
+  static constexpr int kRowBlock = kSlabs * 1024;      // one 8-key block of a K/V tile, all slabs
   static constexpr int kQBytes = kSlabs * kSlab;
-  static constexpr int kKVTile = kSlabs * kSlab;       // K or V tile (128 keys)
-  static constexpr int kStageBytes = 2 * kKVTile;
+  static constexpr int kKVTile = kBN * D * 2;          // K or V tile (128 keys)
   static constexpr int kPBytes = 2 * kSlab;            // P: 128 rows x 128 keys
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQBytes;
-  static constexpr int kPOff = kKVOff + kNS * kStageBytes;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + kNS * kKVTile;
+  static constexpr int kPOff = kVOff + kNS * kKVTile;
   static constexpr int kBarOff = kPOff + kPBytes;
   static constexpr int kSmem = kBarOff + 16 * 8 + 16 + 1024;  // barriers, TMEM base, alignment slack
   static constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O
   static constexpr uint32_t kOCol = 256;
 };
 
-// barriers
-enum { B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + kNS, B_SFULL = 1 + 2 * kNS, B_PFULL = 3 + 2 * kNS, B_PVDONE = 4 + 2 * kNS,
-       B_COUNT = 5 + 2 * kNS };
+// barriers: K and V stages are filled and freed separately (K(j) is free once
+// S(j) is done, V(j) once PV(j) is done); B_VLAST completes the copies of a
+// last V tile that the TMA warp still has to zero past L before publishing
+enum { B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + kNS, B_VFULL = 1 + 2 * kNS, B_VEMPTY = 1 + 3 * kNS,
+       B_SFULL = 1 + 4 * kNS, B_PFULL = 3 + 4 * kNS, B_PVDONE = 4 + 4 * kNS, B_VLAST = 5 + 4 * kNS,
+       B_COUNT = 6 + 4 * kNS };
+static_assert(B_COUNT <= 16, "barrier slots");
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                      PrefillParams p) {
   using C = PCfg<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int b = blockIdx.z, hk = blockIdx.y;
-  const int G = p.group, Hq = p.num_q_heads, Hkv = p.pool.num_kv_heads;
+  const int G = p.group, Hq = p.num_q_heads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qs = __ldg(p.query_start_loc + b);
   const int qe = __ldg(p.query_start_loc + b + 1);
@@ -119,22 +131,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
   }
 
   unsigned char* q_s = smem + C::kQOff;
-  unsigned char* kv_s = smem + C::kKVOff;
   unsigned char* p_s = smem + C::kPOff;
+  const uint32_t k_base = smem_u32(smem + C::kKOff);
+  const uint32_t v_base = smem_u32(smem + C::kVOff);
   const uint32_t bars = smem_u32(smem + C::kBarOff);
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 16 * 8);
 
   if (tid == 0) {
-    mbar_init(bar(B_QFULL), kLoadThreads);
+    mbar_init(bar(B_QFULL), 32 * kSoftmaxWarps);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(bar(B_KVFULL + s), kLoadThreads);
-      mbar_init(bar(B_KVEMPTY + s), 1);
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL + 0), 1);
     mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL), 32 * kSoftmaxWarps);
     mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_VLAST), 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -145,102 +161,119 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
   const float sl2 = p.scale_log2;
   bool alive = true;
 
-  if (warp >= kLoadWarp0) {
-    // ======================= loaders (cp.async) =======================
-    const int lt = tid - 32 * kLoadWarp0;
+  if (warp == kTmaWarp) {
+    // ======================= TMA producer (one warp) =======================
+    // Per tile each lane < ops copies one page box (keys lane*kpo .. +kpo-1 of
+    // the tile); lane 0 posts the byte count of the boxes actually issued.
+    // Every lane waits on the ring barriers in the same order, one phase at a
+    // time, and the warp stops as a whole if a wait gives up.
     griddep_wait();  // the pool rows of this step were written by the append kernel
-    constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    // Q: 128 packed rows
-#pragma unroll 4
-    for (int idx = lt; idx < kBM * kChunks; idx += kLoadThreads) {
-      const int r = idx / kChunks, c = idx % kChunks;
-      const int R = row0 + r;
-      const bool ok = R < rows_total;
-      const __nv_bfloat16* src = ok ? qp + row_off(R) + c * 8 : qp;
-      cp_async_16(smem_u32(q_s + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();  // generic-proxy (cp.async) writes -> visible to the tensor core
-    mbar_arrive(bar(B_QFULL));
-    const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(p.pool.key_pool);
-    const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(p.pool.value_pool);
-    const int64_t row_elems = (int64_t)Hkv * D;
+    const int kpo = ps < kBN ? ps : kBN;  // keys per box
+    const int ops = kBN / kpo;
+    const uint32_t box_bytes = (uint32_t)kpo * D * 2;
     const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
-    for (int j = 0; j < nt; ++j) {
-      const int s = j % kNS;
-      if (j > 0) {
-        // publish tile j-1 before blocking on the ring: the MMA warp may need it
-        // (S(j-1)) before it can free the stage tile j goes to
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(bar(B_KVFULL + (j - 1) % kNS));
-      }
-      if (j >= kNS && alive) alive = mbar_wait(bar(B_KVEMPTY + s), (uint32_t)(((j / kNS) - 1) & 1), p.err);
-      unsigned char* st = kv_s + s * C::kStageBytes;
-      // thread lt copies 16-byte chunk (lt % kChunks) of rows r = lt / kChunks + kRowStep * i of
-      // both K and V: one block_table lookup per row, shared by the two tensors
-      constexpr int kRowStep = kLoadThreads / kChunks;
-      const int c = lt % kChunks;
-#pragma unroll 4
-      for (int r = lt / kChunks; r < kBN; r += kRowStep) {
-        const int key = j * kBN + r;
-        const uint32_t dst = smem_u32(st + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-        int64_t off = -1;
-        if (key < L) {
-          const int page = __ldg(bt + (key >> pshift));
-          if (page < 0 || page >= p.pool.num_pages) record_error(p.err, ERR_BLOCK_TABLE, page);
-          else off = (((int64_t)page << pshift) + (key & (ps - 1))) * row_elems + (int64_t)hk * D + c * 8;
+    auto issue = [&](const CUtensorMap* map, uint32_t dst, int j, uint32_t full) {
+      const int key = j * kBN + lane * kpo;
+      bool ok = lane < ops && key < L;
+      int page = 0;
+      if (ok) {
+        page = __ldg(bt + (key >> pshift));
+        if (page < 0 || page >= p.pool.num_pages) {
+          record_error(p.err, ERR_BLOCK_TABLE, page);
+          ok = false;
         }
-        cp_async_16(dst, off >= 0 ? kpool + off : kpool, off >= 0 ? 16 : 0);
-        cp_async_16(dst + C::kKVTile, off >= 0 ? vpool + off : vpool, off >= 0 ? 16 : 0);
       }
-      cp_async_commit();
+      const int cnt = __popc(__ballot_sync(0xffffffffu, ok));
+      if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)cnt * box_bytes);
+      __syncwarp();
+      if (ok) {
+        const int64_t slot = ((int64_t)page << pshift) + (key & (ps - 1));
+        tma_load_5d(dst + (uint32_t)(lane * (kpo / 8)) * C::kRowBlock, map, 0, 0, 0, (int)(slot >> 3), hk, full);
+      }
+    };
+    for (int j = 0; j < nt && alive; ++j) {
+      const int s = j % kNS;
+      const uint32_t par = (uint32_t)(((j / kNS) - 1) & 1);
+      if (j >= kNS) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_KEMPTY + s), par, p.err));
+      if (!alive) break;
+      issue(&tmap_k, k_base + s * C::kKVTile, j, bar(B_KFULL + s));
+      if (j >= kNS) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VEMPTY + s), par, p.err));
+      if (!alive) break;
+      const uint32_t vdst = v_base + s * C::kKVTile;
+      const int valid = L - j * kBN;  // keys of this tile below L (>= 1)
+      if (valid >= kBN) {
+        issue(&tmap_v, vdst, j, bar(B_VFULL + s));
+      } else {
+        // last tile: slots valid..127 must hold zeros (they meet P = 0, and
+        // the pool there may hold anything, NaN included)
+        issue(&tmap_v, vdst, j, bar(B_VLAST));
+        alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VLAST), 0, p.err));
+        unsigned char* vt = smem + C::kVOff + s * C::kKVTile;
+        const int chunks = (kBN - valid) * (D / 8);  // 16-byte chunks to clear
+        for (int idx = lane; idx < chunks; idx += 32) {
+          const int k = valid + idx / (D / 8), c = idx % (D / 8);
+          *reinterpret_cast<uint4*>(vt + (k >> 3) * C::kRowBlock + (c >> 3) * 1024 + (k & 7) * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_VFULL + s));
+      }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(bar(B_KVFULL + (nt - 1) % kNS));
   }
 
   if (warp == kMmaWarp && lane == 0) {
     // ======================= MMA issuer =======================
+    // S(ns) may be issued once K(ns) is loaded and ns <= np + 1 (its TMEM
+    // buffer held S(ns-2), whose softmax PV(ns-2) has consumed); PV(np) once
+    // V(np) is loaded and P(np) is written.  Whichever is ready goes first.
     const uint32_t q_addr = smem_u32(q_s);
-    const uint32_t kv_addr = smem_u32(kv_s);
     const uint32_t p_addr = smem_u32(p_s);
     constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
     constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
-    auto issue_s = [&](int j) {  // S[j & 1] = Q K_j^T
-      const uint32_t k_addr = kv_addr + (j % kNS) * C::kStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-        umma_bf16(tmem + (j & 1) * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
-                  umma_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
-      }
-      umma_commit(bar(B_SFULL + (j & 1)));
-    };
     if (alive) alive = mbar_wait(bar(B_QFULL), 0, p.err);
-    for (int j = 0; j < nt; ++j) {
-      if (j == 0) {
-        if (alive) alive = mbar_wait(bar(B_KVFULL), 0, p.err);
+    int ns = 0, np = 0;
+    unsigned long long t_last = global_ns();
+    while (np < nt) {
+      bool progressed = false;
+      if (ns < nt && ns <= np + 1 &&
+          (!alive || mbar_test(bar(B_KFULL + ns % kNS), (uint32_t)((ns / kNS) & 1)))) {
         tc_fence_after();
-        issue_s(0);
-      }
-      if (j + 1 < nt) {
-        if (alive) alive = mbar_wait(bar(B_KVFULL + (j + 1) % kNS), (uint32_t)(((j + 1) / kNS) & 1), p.err);
-        tc_fence_after();
-        issue_s(j + 1);
-      }
-      if (alive) alive = mbar_wait(bar(B_PFULL), (uint32_t)(j & 1), p.err);
-      tc_fence_after();
-      const uint32_t v_addr = kv_addr + (j % kNS) * C::kStageBytes + C::kKVTile;
+        const uint32_t k_addr = k_base + (ns % kNS) * C::kKVTile;
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {  // O += P V over 16-key steps
-        umma_bf16(tmem + C::kOCol, umma_desc_sw128(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
-                  umma_desc_sw128(v_addr + kk * 16 * 128, kSlab, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {  // S[ns & 1] = Q K^T over 16-dim steps
+          umma_bf16(tmem + (ns & 1) * kBN, umma_desc_sw128(q_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+                    umma_desc_sw128(k_addr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kRowBlock), idesc_s, kk > 0);
+        }
+        umma_commit(bar(B_SFULL + (ns & 1)));
+        umma_commit(bar(B_KEMPTY + ns % kNS));
+        ++ns;
+        progressed = true;
       }
-      umma_commit(bar(B_PVDONE));
-      umma_commit(bar(B_KVEMPTY + j % kNS));
+      if (np < ns && (!alive || (mbar_test(bar(B_PFULL), (uint32_t)(np & 1)) &&
+                                 mbar_test(bar(B_VFULL + np % kNS), (uint32_t)((np / kNS) & 1))))) {
+        tc_fence_after();
+        const uint32_t v_addr = v_base + (np % kNS) * C::kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {  // O += P V over 16-key steps (two 8-key blocks each)
+          umma_bf16(tmem + C::kOCol, umma_desc_sw128(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+                    umma_desc_sw128(v_addr + kk * 2 * C::kRowBlock, 1024, C::kRowBlock), idesc_o,
+                    (np > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(B_PVDONE));
+        umma_commit(bar(B_VEMPTY + np % kNS));
+        ++np;
+        progressed = true;
+      }
+      const unsigned long long now = global_ns();
+      if (progressed) {
+        t_last = now;
+      } else if (alive && now - t_last > kWaitLimitNs) {
+        record_error(p.err, ERR_TIMEOUT, np);
+        alive = false;  // finish without waiting (results are garbage, recorded)
+      } else {
+        __nanosleep(32);
+      }
     }
   }
 
@@ -249,6 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
     const int r = tid;  // row within the tile == TMEM lane
     const int R = row0 + r;
     const bool valid_row = R < rows_total;
+    {  // this thread's Q row into the UMMA A layout (K-major, 128-byte swizzle); zeros past the last row
+      const __nv_bfloat16* src = qp + (valid_row ? row_off(R) : 0);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        cp_async_16(smem_u32(q_s + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8,
+                    valid_row ? 16 : 0);
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_QFULL));
+    }
     const int pos = valid_row ? first + R / G : pos_max;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float m_ref = -INFINITY, l = 0.f;
@@ -257,72 +301,83 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
       tc_fence_after();
       const uint32_t s_addr = lane_base + (j & 1) * kBN;
       const int key0 = j * kBN;
-      const bool need_mask = key0 + kBN - 1 > pos_min;
-      // pass 1: row max of this tile
-      float tmax = -INFINITY;
+      // the whole row of S(j): 128 fp32 in registers, scaled to log2 units in place
+      uint32_t v[kBN / 32][32];
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb) {
-        uint32_t v[32];
-        tmem_ld32(s_addr + cb * 32, v);
-        tmem_wait_ld();
+      for (int cb = 0; cb < kBN / 32; ++cb) tmem_ld32(s_addr + cb * 32, v[cb]);
+      tmem_wait_ld();
+      if (key0 + kBN - 1 > pos_min) {  // a diagonal tile: column c is visible iff c <= pos - key0
+        const int lim = pos - key0;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float sv = __uint_as_float(v[e]) * sl2;
-          const bool vis = !need_mask || key0 + cb * 32 + e <= pos;
-          tmax = fmaxf(tmax, vis ? sv : -INFINITY);
-        }
+        for (int cb = 0; cb < kBN / 32; ++cb)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[cb][e] = __float_as_uint(cb * 32 + e <= lim ? __uint_as_float(v[cb][e]) * sl2 : -INFINITY);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < kBN / 32; ++cb)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[cb][e] = __float_as_uint(__uint_as_float(v[cb][e]) * sl2);
       }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int cb = 0; cb < kBN / 32; ++cb)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[cb][e]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       // reference max: moved only when the row max grows by more than 2^8
       float alpha = 1.f;
       bool rescale = false;
       if (tmax > m_ref + kRescaleThreshold) {
-        alpha = fast_exp2(m_ref - tmax);  // 0 when m_ref is -inf
+        alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - tmax);
         m_ref = tmax;
         l *= alpha;
         rescale = j > 0;
       }
       const float mbase = m_ref == -INFINITY ? 0.f : m_ref;
+      // P = exp2(x - m) packed as bf16 pairs (in place of S); masked x = -inf gives 0
+      float rs[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < kBN / 32; ++cb)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = fast_exp2(__uint_as_float(v[cb][e]) - mbase);
+          const float p1 = fast_exp2(__uint_as_float(v[cb][e + 1]) - mbase);
+          rs[(e >> 1) & 7] += p0 + p1;
+          v[cb][e >> 1] = pack_bf16(p0, p1);
+        }
+      const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       if (j > 0) {  // PV(j-1) must be done before O is touched and P is overwritten
         if (alive) alive = mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), p.err);
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
+#pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + C::kOCol + cb * 32, v);
+          uint32_t o[32];
+          tmem_ld32(lane_base + C::kOCol + cb * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(lane_base + C::kOCol + cb * 32, v);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(lane_base + C::kOCol + cb * 32, o);
         }
         tmem_wait_st();
       }
-      // pass 2: P = exp2(s - m) as bf16 into the UMMA A layout (K-major, 128-byte swizzle)
-      float rsum = 0.f;
+      // P into the UMMA A layout (K-major, 128-byte swizzle): 16 chunks of 8 keys
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb) {
-        uint32_t v[32];
-        tmem_ld32(s_addr + cb * 32, v);
-        tmem_wait_ld();
-        uint32_t pk[16];
+      for (int cb = 0; cb < kBN / 32; ++cb)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int k0 = key0 + cb * 32 + e;
-          const bool v0 = !need_mask || k0 <= pos, v1 = !need_mask || k0 + 1 <= pos;
-          const float p0 = v0 ? fast_exp2(fmaf(__uint_as_float(v[e]), sl2, -mbase)) : 0.f;
-          const float p1 = v1 ? fast_exp2(fmaf(__uint_as_float(v[e + 1]), sl2, -mbase)) : 0.f;
-          rsum += p0 + p1;
-          pk[e >> 1] = pack_bf16(p0, p1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // four 16-byte chunks: keys cb*32 + 8q .. +7
+        for (int q = 0; q < 4; ++q) {
           const int key = cb * 32 + q * 8;
           const int slab = key >> 6, chunk = (key & 63) >> 3;
           *reinterpret_cast<uint4*>(p_s + slab * kSlab + r * 128 + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              make_uint4(v[cb][4 * q], v[cb][4 * q + 1], v[cb][4 * q + 2], v[cb][4 * q + 3]);
         }
-      }
       l += rsum;
       fence_proxy_async_smem();  // P stores -> visible to the tensor core
       tc_fence_before();
@@ -336,17 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
     __nv_bfloat16* orow = outp + (valid_row ? row_off(R) : 0);
 #pragma unroll
     for (int cb = 0; cb < D / 32; ++cb) {
-      uint32_t v[32];
-      tmem_ld32(lane_base + C::kOCol + cb * 32, v);
+      uint32_t o[32];
+      tmem_ld32(lane_base + C::kOCol + cb * 32, o);
       tmem_wait_ld();
       if (valid_row) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 w;
-          w.x = pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+          w.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
           *reinterpret_cast<uint4*>(orow + cb * 32 + q * 8) = w;
         }
       }
@@ -363,12 +418,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillParams p
 template <int D>
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
   using C = PCfg<D>;
+  const int ps = p.pool.page_size;
+  if (ps < 8 || p.pool.page_shift < 0) return cudaErrorInvalidValue;
+  const int kpo = ps < kBN ? ps : kBN;  // keys per TMA box
+  const int64_t rows = p.pool.num_pages * (int64_t)ps;
+  CUtensorMap tk, tv;
+  if (!encode_pool_tmap_blocked(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, kpo / 8) ||
+      !encode_pool_tmap_blocked(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, kpo / 8))
+    return cudaErrorInvalidValue;
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = ((int64_t)p.max_q_len * p.group + kBM - 1) / kBM;
   return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, (unsigned)p.batch), dim3(kThreads),
-                    (size_t)C::kSmem, s, p);
+                    (size_t)C::kSmem, s, tk, tv, p);
 }
 
 }  // namespace

@@ -50,4 +50,20 @@ bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_
   return r == CUDA_SUCCESS;
 }
 
+bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
+                              int box_blocks) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr || rows % 8 != 0) return false;
+  const cuuint64_t slot_stride = (cuuint64_t)num_kv_heads * head_dim * 2;
+  // dims: 64 dims of a slab, slot within an 8-slot block, slabs, blocks, heads
+  cuuint64_t dims[5] = {64, 8, (cuuint64_t)(head_dim / 64), (cuuint64_t)(rows / 8), (cuuint64_t)num_kv_heads};
+  cuuint64_t strides[4] = {slot_stride, 128, 8 * slot_stride, (cuuint64_t)head_dim * 2};
+  cuuint32_t box[5] = {64, 8, (cuuint32_t)(head_dim / 64), (cuuint32_t)box_blocks, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa

@@ -233,7 +233,7 @@ def test_prefill_ragged(cuda_device, hq, hkv, d):
     _check_step(plan, cuda_device, f"prefill {hq}/{hkv}/{d}")
 
 
-@pytest.mark.parametrize("ps", [4, 8, 32])
+@pytest.mark.parametrize("ps", [8, 32, 64, 256])
 def test_prefill_page_sizes(cuda_device, ps):
     plan = wl.chunked_prefill_plan(new=(33, 90, 1), cached=(5, 64, 200), seed=ps, ps=ps)
     _check_step(plan, cuda_device, f"prefill ps={ps}")
