@@ -11,7 +11,7 @@
 // -- row r is query token r / G, query head hk*G + r % G -- so every K/V tile
 // in shared memory serves all G heads that read it.  Keys come in tiles of
 // 128.
-// * 1 TMA warp stages K/V tiles (2-stage rings) page by page: its lanes look
+// * 1 TMA warp stages K/V tiles (3-stage rings) page by page: its lanes look
 //   up one page each in block_table and issue one box per page (a whole
 //   128-key tile when pages hold >= 128 slots), so a tile costs 128 /
 //   min(page_size, 128) copies.  The 5-D view of the pool lands each box as
@@ -20,14 +20,16 @@
 //   for V.  Slots at or past L_b in the last tile are zeroed in V.
 // * 1 MMA thread issues tcgen05.mma: S = Q K^T (M 128, N 128, fp32 in TMEM,
 //   double-buffered so S(j+1) overlaps the softmax of S(j)) and O += P V
-//   (M 128, N head_dim, fp32 in TMEM), each committed to mbarriers.  It
+//   (M 128, N head_dim, fp32 in TMEM, P from TMEM), each committed to
+//   mbarriers.  It
 //   issues whichever of the next S and the next PV is ready first.
 // * 4 softmax warps own one TMEM lane (= one row) per thread: they stage their
 //   own Q row once (cp.async), then per key tile tcgen05.ld the row of S,
 //   apply the causal mask, run the online softmax in the log2 domain with a
 //   lazily updated reference max (O and l are rescaled in TMEM only when the
-//   row max grows by more than 2^8), write P to shared memory as bf16 in the
-//   UMMA A layout, and at the end write O / l to global as bf16.
+//   row max grows by more than 2^8), write P as bf16 back to TMEM (double
+//   buffered; PV reads its A operand from there), and at the end write O / l
+//   to global as bf16.
 // Fully masked key tiles are never loaded or multiplied.
 #include <math.h>
 
@@ -42,15 +44,18 @@ namespace {
 
 constexpr int kBM = 128;             // packed query rows per CTA (TMEM lanes)
 constexpr int kBN = 128;             // keys per tile
-constexpr int kNS = 2;               // K/V ring stages
+constexpr int kNSK = 3;              // K ring stages
+constexpr int kNSV = 3;              // V ring stages
 constexpr int kSoftmaxWarps = 4;     // warps 0..3 (TMEM lane quarters 0..3)
 constexpr int kMmaWarp = 4;
 constexpr int kTmaWarp = 5;
 // 6 warps: at most 2 per SM sub-partition, so each thread may hold 255
 // registers (the softmax keeps a whole 128-column row of S in registers)
 constexpr int kThreads = 32 * 6;
-constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row Q or P tile (16 KB)
+constexpr int kSlab = kBM * 128;     // one 64-column slab of the 128-row Q tile (16 KB)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+constexpr int kBarSlots = 24;
 
 template <int D>
 struct PCfg {
@@ -58,24 +63,27 @@ struct PCfg {
   static constexpr int kRowBlock = kSlabs * 1024;      // one 8-key block of a K/V tile, all slabs
   static constexpr int kQBytes = kSlabs * kSlab;
   static constexpr int kKVTile = kBN * D * 2;          // K or V tile (128 keys)
-  static constexpr int kPBytes = 2 * kSlab;            // P: 128 rows x 128 keys
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
-  static constexpr int kVOff = kKOff + kNS * kKVTile;
-  static constexpr int kPOff = kVOff + kNS * kKVTile;
-  static constexpr int kBarOff = kPOff + kPBytes;
-  static constexpr int kSmem = kBarOff + 16 * 8 + 16 + 1024;  // barriers, TMEM base, alignment slack
-  static constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O
+  static constexpr int kVOff = kKOff + kNSK * kKVTile;
+  static constexpr int kPageOff = kVOff + kNSV * kKVTile;  // [8 tiles][32 lanes] page ids seen by the TMA warp
+  static constexpr int kBarOff = kPageOff + 8 * 32 * 4;
+  static constexpr int kSmem = kBarOff + kBarSlots * 8 + 16 + 1024;  // barriers, TMEM base, alignment slack
+  static constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O | P0 | P1
   static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kPCol = 384;               // P(j) as bf16 pairs: 64 columns at kPCol + (j & 1) * 64
 };
 
 // barriers: K and V stages are filled and freed separately (K(j) is free once
-// S(j) is done, V(j) once PV(j) is done); B_VLAST completes the copies of a
-// last V tile that the TMA warp still has to zero past L before publishing
-enum { B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 1 + kNS, B_VFULL = 1 + 2 * kNS, B_VEMPTY = 1 + 3 * kNS,
-       B_SFULL = 1 + 4 * kNS, B_PFULL = 3 + 4 * kNS, B_PVDONE = 4 + 4 * kNS, B_VLAST = 5 + 4 * kNS,
-       B_COUNT = 6 + 4 * kNS };
-static_assert(B_COUNT <= 16, "barrier slots");
+// S(j) is done, V(j) once PV(j) is done); S, P and PV-done each have one
+// barrier per TMEM buffer (tile j uses j & 1), which keeps every parity
+// waiter within one phase of its barrier: S(j+2) is issued only after PV(j),
+// and PV(j+1) only after P(j+1).  B_VLAST completes the copies of a last V
+// tile that the TMA warp still has to zero past L before publishing it.
+enum { B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + kNSK, B_VFULL = B_KEMPTY + kNSK, B_VEMPTY = B_VFULL + kNSV,
+       B_SFULL = B_VEMPTY + kNSV, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2, B_VLAST = B_PVDONE + 2,
+       B_COUNT = B_VLAST + 1 };
+static_assert(B_COUNT <= kBarSlots, "barrier slots");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -131,25 +139,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   unsigned char* q_s = smem + C::kQOff;
-  unsigned char* p_s = smem + C::kPOff;
   const uint32_t k_base = smem_u32(smem + C::kKOff);
   const uint32_t v_base = smem_u32(smem + C::kVOff);
   const uint32_t bars = smem_u32(smem + C::kBarOff);
   auto bar = [&](int i) { return bars + 8u * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 16 * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + kBarSlots * 8);
 
   if (tid == 0) {
     mbar_init(bar(B_QFULL), 32 * kSoftmaxWarps);
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kNSK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < kNSV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
     }
     mbar_init(bar(B_SFULL + 0), 1);
     mbar_init(bar(B_SFULL + 1), 1);
-    mbar_init(bar(B_PFULL), 32 * kSoftmaxWarps);
-    mbar_init(bar(B_PVDONE), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_PFULL + i), 32 * kSoftmaxWarps);
+      mbar_init(bar(B_PVDONE + i), 1);
+    }
     mbar_init(bar(B_VLAST), 1);
     fence_mbar_init();
   }
@@ -164,61 +175,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kTmaWarp) {
     // ======================= TMA producer (one warp) =======================
     // Per tile each lane < ops copies one page box (keys lane*kpo .. +kpo-1 of
-    // the tile); lane 0 posts the byte count of the boxes actually issued.
-    // Every lane waits on the ring barriers in the same order, one phase at a
-    // time, and the warp stops as a whole if a wait gives up.
+    // the tile); lane 0 posts the byte count of the boxes actually issued.  K
+    // and V are issued independently, each as soon as its ring slot is free
+    // (polled by lane 0, the result shared with the warp so that all lanes take
+    // the same path).  The page ids of tile j+1 are read while tile j is
+    // issued, and a V tile reuses the ids its K tile looked up.
     griddep_wait();  // the pool rows of this step were written by the append kernel
     const int kpo = ps < kBN ? ps : kBN;  // keys per box
     const int ops = kBN / kpo;
     const uint32_t box_bytes = (uint32_t)kpo * D * 2;
     const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
-    auto issue = [&](const CUtensorMap* map, uint32_t dst, int j, uint32_t full) {
+    int* page_ring = reinterpret_cast<int*>(smem + C::kPageOff);
+    auto fetch = [&](int j) {  // raw block_table entry of this lane's box in tile j, -1 if none
       const int key = j * kBN + lane * kpo;
-      bool ok = lane < ops && key < L;
-      int page = 0;
-      if (ok) {
-        page = __ldg(bt + (key >> pshift));
-        if (page < 0 || page >= p.pool.num_pages) {
-          record_error(p.err, ERR_BLOCK_TABLE, page);
-          ok = false;
-        }
-      }
+      return (j < nt && lane < ops && key < L) ? __ldg(bt + (key >> pshift)) : -1;
+    };
+    auto issue = [&](const CUtensorMap* map, uint32_t dst, int j, int page, uint32_t full) {
+      const bool ok = page >= 0;
       const int cnt = __popc(__ballot_sync(0xffffffffu, ok));
       if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)cnt * box_bytes);
       __syncwarp();
       if (ok) {
-        const int64_t slot = ((int64_t)page << pshift) + (key & (ps - 1));
+        const int64_t slot = ((int64_t)page << pshift) + ((j * kBN + lane * kpo) & (ps - 1));
         tma_load_5d(dst + (uint32_t)(lane * (kpo / 8)) * C::kRowBlock, map, 0, 0, 0, (int)(slot >> 3), hk, full);
       }
     };
-    for (int j = 0; j < nt && alive; ++j) {
-      const int s = j % kNS;
-      const uint32_t par = (uint32_t)(((j / kNS) - 1) & 1);
-      if (j >= kNS) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_KEMPTY + s), par, p.err));
-      if (!alive) break;
-      issue(&tmap_k, k_base + s * C::kKVTile, j, bar(B_KFULL + s));
-      if (j >= kNS) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VEMPTY + s), par, p.err));
-      if (!alive) break;
-      const uint32_t vdst = v_base + s * C::kKVTile;
-      const int valid = L - j * kBN;  // keys of this tile below L (>= 1)
-      if (valid >= kBN) {
-        issue(&tmap_v, vdst, j, bar(B_VFULL + s));
-      } else {
-        // last tile: slots valid..127 must hold zeros (they meet P = 0, and
-        // the pool there may hold anything, NaN included)
-        issue(&tmap_v, vdst, j, bar(B_VLAST));
-        alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VLAST), 0, p.err));
-        unsigned char* vt = smem + C::kVOff + s * C::kKVTile;
-        const int chunks = (kBN - valid) * (D / 8);  // 16-byte chunks to clear
-        for (int idx = lane; idx < chunks; idx += 32) {
-          const int k = valid + idx / (D / 8), c = idx % (D / 8);
-          *reinterpret_cast<uint4*>(vt + (k >> 3) * C::kRowBlock + (c >> 3) * 1024 + (k & 7) * 128 + (c & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+    auto slot_free = [&](int i) {  // lane 0 polls, the warp agrees
+      int t = 0;
+      if (lane == 0) t = mbar_test(bar(i >> 1), (uint32_t)(i & 1)) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, t, 0) != 0;
+    };
+    int jk = 0, jv = 0;
+    int raw = fetch(0);
+    unsigned long long t_last = global_ns();
+    while (jv < nt && alive) {
+      bool progressed = false;
+      if (jk < nt && (jk < kNSK || slot_free(((B_KEMPTY + jk % kNSK) << 1) | (((jk / kNSK) - 1) & 1)))) {
+        int page = raw;
+        if (lane < ops && jk * kBN + lane * kpo < L) {
+          if (page < 0 || page >= p.pool.num_pages) {
+            record_error(p.err, ERR_BLOCK_TABLE, page);
+            page = -1;
+          }
+        } else {
+          page = -1;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_VFULL + s));
+        page_ring[(jk & 7) * 32 + lane] = page;
+        issue(&tmap_k, k_base + (jk % kNSK) * C::kKVTile, jk, page, bar(B_KFULL + jk % kNSK));
+        ++jk;
+        raw = fetch(jk);
+        progressed = true;
       }
+      if (jv < jk && (jv < kNSV || slot_free(((B_VEMPTY + jv % kNSV) << 1) | (((jv / kNSV) - 1) & 1)))) {
+        const int s = jv % kNSV;
+        const int page = page_ring[(jv & 7) * 32 + lane];
+        const uint32_t vdst = v_base + s * C::kKVTile;
+        const int valid = L - jv * kBN;  // keys of this tile below L (>= 1)
+        if (valid >= kBN) {
+          issue(&tmap_v, vdst, jv, page, bar(B_VFULL + s));
+        } else {
+          // last tile: slots valid..127 must hold zeros (they meet P = 0, and
+          // the pool there may hold anything, NaN included)
+          issue(&tmap_v, vdst, jv, page, bar(B_VLAST));
+          alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VLAST), 0, p.err));
+          unsigned char* vt = smem + C::kVOff + s * C::kKVTile;
+          const int chunks = (kBN - valid) * (D / 8);  // 16-byte chunks to clear
+          for (int idx = lane; idx < chunks; idx += 32) {
+            const int k = valid + idx / (D / 8), c = idx % (D / 8);
+            *reinterpret_cast<uint4*>(vt + (k >> 3) * C::kRowBlock + (c >> 3) * 1024 + (k & 7) * 128 +
+                                      (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_VFULL + s));
+        }
+        ++jv;
+        progressed = true;
+      }
+      int give_up = 0;
+      if (lane == 0) {
+        const unsigned long long now = global_ns();
+        if (progressed) {
+          t_last = now;
+        } else if (now - t_last > kWaitLimitNs) {
+          record_error(p.err, ERR_TIMEOUT, jv);
+          give_up = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) alive = false;
+      if (!progressed) __nanosleep(64);
     }
   }
 
@@ -228,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // buffer held S(ns-2), whose softmax PV(ns-2) has consumed); PV(np) once
     // V(np) is loaded and P(np) is written.  Whichever is ready goes first.
     const uint32_t q_addr = smem_u32(q_s);
-    const uint32_t p_addr = smem_u32(p_s);
     constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
     constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
     if (alive) alive = mbar_wait(bar(B_QFULL), 0, p.err);
@@ -237,31 +281,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (np < nt) {
       bool progressed = false;
       if (ns < nt && ns <= np + 1 &&
-          (!alive || mbar_test(bar(B_KFULL + ns % kNS), (uint32_t)((ns / kNS) & 1)))) {
+          (!alive || mbar_test(bar(B_KFULL + ns % kNSK), (uint32_t)((ns / kNSK) & 1)))) {
         tc_fence_after();
-        const uint32_t k_addr = k_base + (ns % kNS) * C::kKVTile;
+        const uint32_t k_addr = k_base + (ns % kNSK) * C::kKVTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {  // S[ns & 1] = Q K^T over 16-dim steps
           umma_bf16(tmem + (ns & 1) * kBN, umma_desc_sw128(q_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
                     umma_desc_sw128(k_addr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kRowBlock), idesc_s, kk > 0);
         }
         umma_commit(bar(B_SFULL + (ns & 1)));
-        umma_commit(bar(B_KEMPTY + ns % kNS));
+        umma_commit(bar(B_KEMPTY + ns % kNSK));
         ++ns;
         progressed = true;
       }
-      if (np < ns && (!alive || (mbar_test(bar(B_PFULL), (uint32_t)(np & 1)) &&
-                                 mbar_test(bar(B_VFULL + np % kNS), (uint32_t)((np / kNS) & 1))))) {
+      if (np < ns && (!alive || (mbar_test(bar(B_PFULL + (np & 1)), (uint32_t)((np >> 1) & 1)) &&
+                                 mbar_test(bar(B_VFULL + np % kNSV), (uint32_t)((np / kNSV) & 1))))) {
         tc_fence_after();
-        const uint32_t v_addr = v_base + (np % kNS) * C::kKVTile;
+        const uint32_t v_addr = v_base + (np % kNSV) * C::kKVTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {  // O += P V over 16-key steps (two 8-key blocks each)
-          umma_bf16(tmem + C::kOCol, umma_desc_sw128(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
-                    umma_desc_sw128(v_addr + kk * 2 * C::kRowBlock, 1024, C::kRowBlock), idesc_o,
-                    (np > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + C::kOCol, tmem + C::kPCol + (np & 1) * 64 + kk * 8,
+                       umma_desc_sw128(v_addr + kk * 2 * C::kRowBlock, 1024, C::kRowBlock), idesc_o,
+                       (np > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bar(B_PVDONE));
-        umma_commit(bar(B_VEMPTY + np % kNS));
+        umma_commit(bar(B_PVDONE + (np & 1)));
+        umma_commit(bar(B_VEMPTY + np % kNSV));
         ++np;
         progressed = true;
       }
@@ -352,11 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[cb][e >> 1] = pack_bf16(p0, p1);
         }
       const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      if (j > 0) {  // PV(j-1) must be done before O is touched and P is overwritten
-        if (alive) alive = mbar_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), p.err);
-        tc_fence_after();
-      }
+      // O is rescaled in place only when some row of the warp moved its
+      // reference max; PV(j-1) must have finished with O first.  (S(j) being
+      // complete already implies PV(j-2) is, so P's buffer j & 1 is free.)
       if (__any_sync(0xffffffffu, rescale)) {
+        if (alive) alive = mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), p.err);
+        tc_fence_after();
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t o[32];
@@ -366,25 +411,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(lane_base + C::kOCol + cb * 32, o);
         }
-        tmem_wait_st();
       }
-      // P into the UMMA A layout (K-major, 128-byte swizzle): 16 chunks of 8 keys
+      // P(j) into TMEM as the A operand of PV(j): 64 keys per 32 columns
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int key = cb * 32 + q * 8;
-          const int slab = key >> 6, chunk = (key & 63) >> 3;
-          *reinterpret_cast<uint4*>(p_s + slab * kSlab + r * 128 + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(v[cb][4 * q], v[cb][4 * q + 1], v[cb][4 * q + 2], v[cb][4 * q + 3]);
+        for (int i = 0; i < 16; ++i) {
+          w[i] = v[2 * h][i];
+          w[16 + i] = v[2 * h + 1][i];
         }
+        tmem_st32(lane_base + C::kPCol + (j & 1) * 64 + h * 32, w);
+      }
+      tmem_wait_st();
       l += rsum;
-      fence_proxy_async_smem();  // P stores -> visible to the tensor core
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + (j & 1)));
     }
     // ---- epilogue: O / l -> bf16 ----
-    if (alive) alive = mbar_wait(bar(B_PVDONE), (uint32_t)((nt - 1) & 1), p.err);
+    if (alive) alive = mbar_wait(bar(B_PVDONE + ((nt - 1) & 1)), (uint32_t)(((nt - 1) >> 1) & 1), p.err);
     tc_fence_after();
     griddep_wait();  // before the first global write
     const float inv = l > 0.f ? 1.f / l : 0.f;
