@@ -7,29 +7,33 @@
 // it works", step 3).  Token i of sequence b sits at absolute position
 // p = L_b - n_b + i and sees keys 0..p, read from the pages in block_table.
 //
-// Tiling (GB300-first): a CTA owns 128 packed rows of one (sequence, KV head)
-// -- row r is query token r / G, query head hk*G + r % G -- so every K/V tile
-// in shared memory serves all G heads that read it.  Keys come in tiles of
+// Tiling (GB300-first): a CTA owns 256 packed rows of one (sequence, KV head)
+// -- row r is query token r / G, query head hk*G + r % G -- as two 128-row
+// query tiles A and B that share every K/V tile staged in shared memory, so
+// each byte brought in feeds twice the tensor-core work (the copies, not the
+// tensor core, bound a single-tile CTA: with ~2 us of loaded L2 latency, the
+// bytes a CTA can keep in flight cap its tile rate).  Keys come in tiles of
 // 128.
-// * 1 TMA warp stages K/V tiles (3-stage rings) page by page: its lanes look
-//   up one page each in block_table and issue one box per page (a whole
-//   128-key tile when pages hold >= 128 slots), so a tile costs 128 /
-//   min(page_size, 128) copies.  The 5-D view of the pool lands each box as
-//   [8-slot block][64-dim slab][8 slots][128 B], i.e. 8-key row groups at one
-//   uniform stride: exactly a K-major UMMA operand for K and an MN-major one
-//   for V.  Slots at or past L_b in the last tile are zeroed in V.
-// * 1 MMA thread issues tcgen05.mma: S = Q K^T (M 128, N 128, fp32 in TMEM,
-//   double-buffered so S(j+1) overlaps the softmax of S(j)) and O += P V
-//   (M 128, N head_dim, fp32 in TMEM, P from TMEM), each committed to
-//   mbarriers.  It
-//   issues whichever of the next S and the next PV is ready first.
-// * 4 softmax warps own one TMEM lane (= one row) per thread: they stage their
-//   own Q row once (cp.async), then per key tile tcgen05.ld the row of S,
-//   apply the causal mask, run the online softmax in the log2 domain with a
-//   lazily updated reference max (O and l are rescaled in TMEM only when the
-//   row max grows by more than 2^8), write P as bf16 back to TMEM (double
-//   buffered; PV reads its A operand from there), and at the end write O / l
-//   to global as bf16.
+// * 1 TMA warp stages K/V tiles (3- and 2-stage rings) page by page: its
+//   lanes look up one page each in block_table and issue one box per page (a
+//   whole 128-key tile when pages hold >= 128 slots).  The 5-D view of the
+//   pool lands each box as [8-slot block][64-dim slab][8 slots][128 B], i.e.
+//   8-key row groups at one uniform stride: exactly a K-major UMMA operand
+//   for K and an MN-major one for V.  Slots at or past L_b in the last tile
+//   are zeroed in V.
+// * 1 MMA thread issues tcgen05.mma in a fixed order, S_A(0) S_B(0), then per
+//   key tile j: PV_A(j) S_A(j+1) PV_B(j) S_B(j+1), so the tensor core works
+//   on one query tile while the other tile's softmax runs.  S = Q K^T and
+//   O += P V are M 128 with fp32 accumulators in TMEM; P is bf16 in TMEM,
+//   written over the columns of S it came from, and read by PV as its A
+//   operand.  (tcgen05 operations of one thread execute in issue order, so
+//   S(j+1) overwrites P(j) only after PV(j) has read it.)
+// * 2 softmax warpgroups, one per query tile, own one TMEM lane (= one row)
+//   per thread: they stage their own Q row once (cp.async), then per key tile
+//   read the row of S from TMEM twice (the max, then exp2 and P), apply the
+//   causal mask, run the online softmax in the log2 domain with a lazily
+//   updated reference max (O and l are rescaled in TMEM only when the row
+//   max grows by more than 2^8), and at the end write O / l as bf16.
 // Fully masked key tiles are never loaded or multiplied.
 #include <math.h>
 
@@ -42,46 +46,45 @@ namespace pa {
 
 namespace {
 
-constexpr int kBM = 128;             // packed query rows per CTA (TMEM lanes)
+constexpr int kBM = 128;             // packed query rows per query tile (TMEM lanes)
+constexpr int kQT = 2;               // query tiles per CTA
 constexpr int kBN = 128;             // keys per tile
 constexpr int kNSK = 3;              // K ring stages
-constexpr int kNSV = 3;              // V ring stages
-constexpr int kSoftmaxWarps = 4;     // warps 0..3 (TMEM lane quarters 0..3)
-constexpr int kMmaWarp = 4;
-constexpr int kTmaWarp = 5;
-// 6 warps: at most 2 per SM sub-partition, so each thread may hold 255
-// registers (the softmax keeps a whole 128-column row of S in registers)
-constexpr int kThreads = 32 * 6;
-constexpr int kSlab = kBM * 128;     // one 64-column slab of the 128-row Q tile (16 KB)
+constexpr int kNSV = 2;              // V ring stages
+constexpr int kMmaWarp = 8;          // warps 0..7: softmax of query tile (warp / 4)
+constexpr int kTmaWarp = 9;
+// 10 warps: 3 on two SM sub-partitions, so at most 168 registers a thread;
+// the softmax holds half a row of S (64 fp32) at a time
+constexpr int kThreads = 32 * 10;
+constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row Q tile (16 KB)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-
 constexpr int kBarSlots = 24;
 
 template <int D>
 struct PCfg {
   static constexpr int kSlabs = D / 64;
   static constexpr int kRowBlock = kSlabs * 1024;      // one 8-key block of a K/V tile, all slabs
-  static constexpr int kQBytes = kSlabs * kSlab;
+  static constexpr int kQBytes = kSlabs * kSlab;       // one Q tile
   static constexpr int kKVTile = kBN * D * 2;          // K or V tile (128 keys)
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQBytes;
+  static constexpr int kKOff = kQT * kQBytes;
   static constexpr int kVOff = kKOff + kNSK * kKVTile;
   static constexpr int kPageOff = kVOff + kNSV * kKVTile;  // [8 tiles][32 lanes] page ids seen by the TMA warp
   static constexpr int kBarOff = kPageOff + 8 * 32 * 4;
   static constexpr int kSmem = kBarOff + kBarSlots * 8 + 16 + 1024;  // barriers, TMEM base, alignment slack
-  static constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O | P0 | P1
-  static constexpr uint32_t kOCol = 256;
-  static constexpr uint32_t kPCol = 384;               // P(j) as bf16 pairs: 64 columns at kPCol + (j & 1) * 64
+  static constexpr uint32_t kTmemCols = 512;           // S_A | S_B | O_A | O_B
+  static constexpr uint32_t kSCol = 0;                 // S of query tile t at kSCol + 128 t (P over its first 64)
+  static constexpr uint32_t kOCol = 256;               // O of query tile t at kOCol + 128 t
 };
 
-// barriers: K and V stages are filled and freed separately (K(j) is free once
-// S(j) is done, V(j) once PV(j) is done); S, P and PV-done each have one
-// barrier per TMEM buffer (tile j uses j & 1), which keeps every parity
-// waiter within one phase of its barrier: S(j+2) is issued only after PV(j),
-// and PV(j+1) only after P(j+1).  B_VLAST completes the copies of a last V
-// tile that the TMA warp still has to zero past L before publishing it.
+// barriers.  K and V stages are filled and freed separately (K(j) is free
+// once both S(j) are done, V(j) once both PV(j) are).  S, P and O-done have
+// one barrier per query tile.  Every parity waiter stays within one phase of
+// its barrier: S_t(j+1) is issued only after PV_t(j), which needs P_t(j).
+// B_VLAST completes the copies of a last V tile that the TMA warp still has
+// to zero past L before publishing it.
 enum { B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + kNSK, B_VFULL = B_KEMPTY + kNSK, B_VEMPTY = B_VFULL + kNSV,
-       B_SFULL = B_VEMPTY + kNSV, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2, B_VLAST = B_PVDONE + 2,
+       B_SFULL = B_VEMPTY + kNSV, B_PFULL = B_SFULL + kQT, B_ODONE = B_PFULL + kQT, B_VLAST = B_ODONE + kQT,
        B_COUNT = B_VLAST + 1 };
 static_assert(B_COUNT <= kBarSlots, "barrier slots");
 
@@ -112,15 +115,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (n > p.max_q_len && tid == 0 && hk == 0 && blockIdx.x == 0) record_error(p.err, ERR_QUERY_LOC, n);
   const int rows_total = n * G;
-  const int tiles = (rows_total + kBM - 1) / kBM;
+  const int tiles = (rows_total + kQT * kBM - 1) / (kQT * kBM);
   const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
   if (tile >= tiles) return;
-  const int row0 = tile * kBM;
   const int first = L - n;  // absolute position of new token 0
-  const int last_row = min(row0 + kBM, rows_total) - 1;
-  const int pos_max = first + last_row / G;
-  const int pos_min = first + row0 / G;
-  const int nt = pos_max >= 0 ? pos_max / kBN + 1 : 0;  // key tiles with a visible key
+  // per query tile t: rows from row0_t, key tiles nt_t with a visible key (0 if the tile has no row)
+  int row0_t[kQT], pmin_t[kQT], nt_t[kQT];
+#pragma unroll
+  for (int t = 0; t < kQT; ++t) {
+    row0_t[t] = (tile * kQT + t) * kBM;
+    const int last_row = min(row0_t[t] + kBM, rows_total) - 1;
+    pmin_t[t] = first + row0_t[t] / G;
+    const int pmax = first + last_row / G;
+    nt_t[t] = (row0_t[t] < rows_total && pmax >= 0) ? pmax / kBN + 1 : 0;
+  }
+  const int nt = max(nt_t[0], nt_t[1]);  // key tiles the CTA loads
 
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
   const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
@@ -129,10 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return ((int64_t)(qs + i) * Hq + (int64_t)hk * G + g) * D;
   };
   griddep_launch_dependents();
-  if (nt == 0) {  // no row of this tile sees any key (invalid input): zeros
+  if (nt == 0) {  // no row of this CTA sees any key (invalid input): zeros
     griddep_wait();
-    for (int idx = tid; idx < kBM * D; idx += kThreads) {
-      const int R = row0 + idx / D;
+    const int r0 = row0_t[0];
+    for (int idx = tid; idx < kQT * kBM * D; idx += kThreads) {
+      const int R = r0 + idx / D;
       if (R < rows_total) outp[row_off(R) + idx % D] = __float2bfloat16_rn(0.f);
     }
     return;
@@ -146,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + kBarSlots * 8);
 
   if (tid == 0) {
-    mbar_init(bar(B_QFULL), 32 * kSoftmaxWarps);
+    mbar_init(bar(B_QFULL), 32 * 8);
     for (int s = 0; s < kNSK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
@@ -155,11 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
     }
-    mbar_init(bar(B_SFULL + 0), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_PFULL + i), 32 * kSoftmaxWarps);
-      mbar_init(bar(B_PVDONE + i), 1);
+    for (int t = 0; t < kQT; ++t) {
+      mbar_init(bar(B_SFULL + t), 1);
+      mbar_init(bar(B_PFULL + t), 32 * 4);
+      mbar_init(bar(B_ODONE + t), 1);
     }
     mbar_init(bar(B_VLAST), 1);
     fence_mbar_init();
@@ -180,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (polled by lane 0, the result shared with the warp so that all lanes take
     // the same path).  The page ids of tile j+1 are read while tile j is
     // issued, and a V tile reuses the ids its K tile looked up.
-    griddep_wait();  // the pool rows of this step were written by the append kernel
     const int kpo = ps < kBN ? ps : kBN;  // keys per box
     const int ops = kBN / kpo;
     const uint32_t box_bytes = (uint32_t)kpo * D * 2;
@@ -206,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, t, 0) != 0;
     };
     int jk = 0, jv = 0;
-    int raw = fetch(0);
+    int raw = fetch(0);  // block_table is an input, not written by the append kernel
+    griddep_wait();      // the pool rows of this step were written by the append kernel
     unsigned long long t_last = global_ns();
     while (jv < nt && alive) {
       bool progressed = false;
@@ -267,111 +276,137 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+
   if (warp == kMmaWarp && lane == 0) {
     // ======================= MMA issuer =======================
-    // S(ns) may be issued once K(ns) is loaded and ns <= np + 1 (its TMEM
-    // buffer held S(ns-2), whose softmax PV(ns-2) has consumed); PV(np) once
-    // V(np) is loaded and P(np) is written.  Whichever is ready goes first.
-    const uint32_t q_addr = smem_u32(q_s);
+    // Fixed order S_A(0) S_B(0), then per key tile j: PV_A(j) S_A(j+1)
+    // PV_B(j) S_B(j+1), skipping the key tiles a query tile does not see: the
+    // two query tiles alternate on the tensor core, each one's softmax running
+    // while the other's products do.  The first S of a key tile waits for K,
+    // the first PV for V; the last S (PV) of a key tile frees its K (V) stage.
     constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
     constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
+    // descriptors at the base of each operand; a K step adds its byte offset / 16
+    // to the start-address field (every address stays below 256 KB, so no carry)
+    const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s), 16, 1024);
+    const uint64_t k_desc = umma_desc_sw128(k_base, 16, C::kRowBlock);
+    const uint64_t v_desc = umma_desc_sw128(v_base, 1024, C::kRowBlock);
     if (alive) alive = mbar_wait(bar(B_QFULL), 0, p.err);
-    int ns = 0, np = 0;
-    unsigned long long t_last = global_ns();
-    while (np < nt) {
-      bool progressed = false;
-      if (ns < nt && ns <= np + 1 &&
-          (!alive || mbar_test(bar(B_KFULL + ns % kNSK), (uint32_t)((ns / kNSK) & 1)))) {
+    const int nt0 = nt_t[0], nt1 = nt_t[1];
+    auto issue_s = [&](int t, int j) {
+      const int sk = j % kNSK;
+      if (t == 0 || j >= nt0) {  // first S of key tile j
+        if (alive) alive = mbar_wait(bar(B_KFULL + sk), (uint32_t)((j / kNSK) & 1), p.err);
         tc_fence_after();
-        const uint32_t k_addr = k_base + (ns % kNSK) * C::kKVTile;
+      }
+      const uint64_t qd = q_desc + (uint64_t)((t * C::kQBytes) >> 4);
+      const uint64_t kd = k_desc + (uint64_t)((sk * C::kKVTile) >> 4);
+      const uint32_t s_tm = tmem + C::kSCol + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S[ns & 1] = Q K^T over 16-dim steps
-          umma_bf16(tmem + (ns & 1) * kBN, umma_desc_sw128(q_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
-                    umma_desc_sw128(k_addr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kRowBlock), idesc_s, kk > 0);
-        }
-        umma_commit(bar(B_SFULL + (ns & 1)));
-        umma_commit(bar(B_KEMPTY + ns % kNSK));
-        ++ns;
-        progressed = true;
+      for (int kk = 0; kk < D / 16; ++kk)  // S_t = Q_t K^T over 16-dim steps
+        umma_bf16(s_tm, qd + (uint64_t)(((kk >> 2) * kSlab + (kk & 3) * 32) >> 4),
+                  kd + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+      umma_commit(bar(B_SFULL + t));
+      if (t == 1 || j >= nt1) umma_commit(bar(B_KEMPTY + sk));  // last S of key tile j
+    };
+    auto issue_pv = [&](int t, int j) {
+      const int sv = j % kNSV;
+      if (alive) alive = mbar_wait(bar(B_PFULL + t), (uint32_t)(j & 1), p.err);
+      if (t == 0 || j >= nt0) {  // first PV of key tile j
+        if (alive) alive = mbar_wait(bar(B_VFULL + sv), (uint32_t)((j / kNSV) & 1), p.err);
       }
-      if (np < ns && (!alive || (mbar_test(bar(B_PFULL + (np & 1)), (uint32_t)((np >> 1) & 1)) &&
-                                 mbar_test(bar(B_VFULL + np % kNSV), (uint32_t)((np / kNSV) & 1))))) {
-        tc_fence_after();
-        const uint32_t v_addr = v_base + (np % kNSV) * C::kKVTile;
+      tc_fence_after();
+      const uint64_t vd = v_desc + (uint64_t)((sv * C::kKVTile) >> 4);
+      const uint32_t s_tm = tmem + C::kSCol + t * 128;
+      const uint32_t o_tm = tmem + C::kOCol + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {  // O += P V over 16-key steps (two 8-key blocks each)
-          umma_bf16_ts(tmem + C::kOCol, tmem + C::kPCol + (np & 1) * 64 + kk * 8,
-                       umma_desc_sw128(v_addr + kk * 2 * C::kRowBlock, 1024, C::kRowBlock), idesc_o,
-                       (np > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_PVDONE + (np & 1)));
-        umma_commit(bar(B_VEMPTY + np % kNSV));
-        ++np;
-        progressed = true;
-      }
-      const unsigned long long now = global_ns();
-      if (progressed) {
-        t_last = now;
-      } else if (alive && now - t_last > kWaitLimitNs) {
-        record_error(p.err, ERR_TIMEOUT, np);
-        alive = false;  // finish without waiting (results are garbage, recorded)
-      } else {
-        __nanosleep(32);
-      }
+      for (int kk = 0; kk < kBN / 16; ++kk)  // O_t += P_t V over 16-key steps (two 8-key blocks each)
+        umma_bf16_ts(o_tm, s_tm + kk * 8, vd + (uint64_t)((kk * 2 * C::kRowBlock) >> 4), idesc_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+      if (j == (t ? nt1 : nt0) - 1) umma_commit(bar(B_ODONE + t));
+      if (t == 1 || j >= nt1) umma_commit(bar(B_VEMPTY + sv));  // last PV of key tile j
+    };
+    if (nt0 > 0) issue_s(0, 0);
+    if (nt1 > 0) issue_s(1, 0);
+    for (int j = 0; j < nt; ++j) {
+      if (j < nt0) issue_pv(0, j);
+      if (j + 1 < nt0) issue_s(0, j + 1);
+      if (j < nt1) issue_pv(1, j);
+      if (j + 1 < nt1) issue_s(1, j + 1);
     }
   }
 
-  if (warp < kSoftmaxWarps) {
+  if (warp < 4 * kQT) {
     // ======================= softmax: one TMEM lane (row) per thread =======================
-    const int r = tid;  // row within the tile == TMEM lane
-    const int R = row0 + r;
+    const int t = warp >> 2;                 // query tile
+    const int r = tid & (kBM - 1);           // row within the tile == TMEM lane
+    const int R = (t ? row0_t[1] : row0_t[0]) + r;
     const bool valid_row = R < rows_total;
+    const int ntt = t ? nt_t[1] : nt_t[0];
+    const int pmin = t ? pmin_t[1] : pmin_t[0];
     {  // this thread's Q row into the UMMA A layout (K-major, 128-byte swizzle); zeros past the last row
+      unsigned char* qt = q_s + t * C::kQBytes;
       const __nv_bfloat16* src = qp + (valid_row ? row_off(R) : 0);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c)
-        cp_async_16(smem_u32(q_s + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8,
+        cp_async_16(smem_u32(qt + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8,
                     valid_row ? 16 : 0);
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
       mbar_arrive(bar(B_QFULL));
     }
-    const int pos = valid_row ? first + R / G : pos_max;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int pos = valid_row ? first + R / G : -1;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + C::kSCol + t * 128;
+    const uint32_t o_col = lane_base + C::kOCol + t * 128;
     float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < nt; ++j) {
-      if (alive) alive = mbar_wait(bar(B_SFULL + (j & 1)), (uint32_t)((j >> 1) & 1), p.err);
+    for (int j = 0; j < ntt; ++j) {
+      if (alive) alive = mbar_wait(bar(B_SFULL + t), (uint32_t)(j & 1), p.err);
       tc_fence_after();
-      const uint32_t s_addr = lane_base + (j & 1) * kBN;
       const int key0 = j * kBN;
-      // the whole row of S(j): 128 fp32 in registers, scaled to log2 units in place
-      uint32_t v[kBN / 32][32];
-#pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb) tmem_ld32(s_addr + cb * 32, v[cb]);
-      tmem_wait_ld();
-      if (key0 + kBN - 1 > pos_min) {  // a diagonal tile: column c is visible iff c <= pos - key0
-        const int lim = pos - key0;
-#pragma unroll
-        for (int cb = 0; cb < kBN / 32; ++cb)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[cb][e] = __float_as_uint(cb * 32 + e <= lim ? __uint_as_float(v[cb][e]) * sl2 : -INFINITY);
-      } else {
-#pragma unroll
-        for (int cb = 0; cb < kBN / 32; ++cb)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[cb][e] = __float_as_uint(__uint_as_float(v[cb][e]) * sl2);
-      }
+      const bool diag = key0 + kBN - 1 > pmin;  // some key of the tile lies past some row's position
+      const int lim = pos - key0;                    // column c is visible iff c <= lim
+      // x = s * scale * log2(e), -inf where masked.  Off the diagonal with a
+      // positive scale (the common case) the max is taken over raw S and
+      // exp2 takes one fused multiply-add: no mask, no separate scaling.
+      const bool plain = !diag && sl2 > 0.f;
+      auto scaled = [&](uint32_t raw, int c) {
+        const float x = __uint_as_float(raw) * sl2;
+        return (!diag || c <= lim) ? x : -INFINITY;
+      };
+      // pass 1: the row max, 64 columns at a time
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      if (plain) {
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb)
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[2][32];
+          tmem_ld32(s_col + h * 64, v[0]);
+          tmem_ld32(s_col + h * 64 + 32, v[1]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[cb][e]));
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[cb][e]));
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[2][32];
+          tmem_ld32(s_col + h * 64, v[0]);
+          tmem_ld32(s_col + h * 64 + 32, v[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], scaled(v[cb][e], h * 64 + cb * 32 + e));
+        }
+      }
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (plain) tmax *= sl2;
       // reference max: moved only when the row max grows by more than 2^8
       float alpha = 1.f;
       bool rescale = false;
@@ -382,63 +417,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = j > 0;
       }
       const float mbase = m_ref == -INFINITY ? 0.f : m_ref;
-      // P = exp2(x - m) packed as bf16 pairs (in place of S); masked x = -inf gives 0
+      // pass 2: P = exp2(x - m) as bf16 pairs, written over the S columns just read
       float rs[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rs[i] = 0.f;
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[2][32];
+        tmem_ld32(s_col + h * 64, v[0]);
+        tmem_ld32(s_col + h * 64 + 32, v[1]);
+        tmem_wait_ld();
+        uint32_t w[32];
+        if (plain) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = fast_exp2(__uint_as_float(v[cb][e]) - mbase);
-          const float p1 = fast_exp2(__uint_as_float(v[cb][e + 1]) - mbase);
-          rs[(e >> 1) & 7] += p0 + p1;
-          v[cb][e >> 1] = pack_bf16(p0, p1);
+          for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(v[cb][e]), sl2, -mbase));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(v[cb][e + 1]), sl2, -mbase));
+              rs[(e >> 1) & 7] += p0 + p1;
+              w[cb * 16 + (e >> 1)] = pack_bf16(p0, p1);
+            }
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = fast_exp2(scaled(v[cb][e], h * 64 + cb * 32 + e) - mbase);
+              const float p1 = fast_exp2(scaled(v[cb][e + 1], h * 64 + cb * 32 + e + 1) - mbase);
+              rs[(e >> 1) & 7] += p0 + p1;
+              w[cb * 16 + (e >> 1)] = pack_bf16(p0, p1);
+            }
         }
-      const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        tmem_st32(s_col + h * 32, w);
+      }
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       // O is rescaled in place only when some row of the warp moved its
-      // reference max; PV(j-1) must have finished with O first.  (S(j) being
-      // complete already implies PV(j-2) is, so P's buffer j & 1 is free.)
+      // reference max.  PV_t(j-1) is complete: S_t(j) was issued after it.
       if (__any_sync(0xffffffffu, rescale)) {
-        if (alive) alive = mbar_wait(bar(B_PVDONE + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), p.err);
-        tc_fence_after();
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t o[32];
-          tmem_ld32(lane_base + C::kOCol + cb * 32, o);
+          tmem_ld32(o_col + cb * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_base + C::kOCol + cb * 32, o);
+          tmem_st32(o_col + cb * 32, o);
         }
-      }
-      // P(j) into TMEM as the A operand of PV(j): 64 keys per 32 columns
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          w[i] = v[2 * h][i];
-          w[16 + i] = v[2 * h + 1][i];
-        }
-        tmem_st32(lane_base + C::kPCol + (j & 1) * 64 + h * 32, w);
       }
       tmem_wait_st();
-      l += rsum;
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + (j & 1)));
+      mbar_arrive(bar(B_PFULL + t));
     }
-    // ---- epilogue: O / l -> bf16 ----
-    if (alive) alive = mbar_wait(bar(B_PVDONE + ((nt - 1) & 1)), (uint32_t)(((nt - 1) >> 1) & 1), p.err);
-    tc_fence_after();
+    // ---- epilogue: O / l -> bf16 (zeros for a tile that sees no key) ----
+    if (ntt > 0) {
+      if (alive) alive = mbar_wait(bar(B_ODONE + t), 0, p.err);
+      tc_fence_after();
+    }
     griddep_wait();  // before the first global write
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = outp + (valid_row ? row_off(R) : 0);
 #pragma unroll
     for (int cb = 0; cb < D / 32; ++cb) {
       uint32_t o[32];
-      tmem_ld32(lane_base + C::kOCol + cb * 32, o);
-      tmem_wait_ld();
+      if (ntt > 0) {
+        tmem_ld32(o_col + cb * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
       if (valid_row) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -474,7 +522,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = ((int64_t)p.max_q_len * p.group + kBM - 1) / kBM;
+  const int64_t tiles = ((int64_t)p.max_q_len * p.group + kQT * kBM - 1) / (kQT * kBM);
   return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, (unsigned)p.batch), dim3(kThreads),
                     (size_t)C::kSmem, s, tk, tv, p);
 }
