@@ -82,7 +82,8 @@ template <int D, int HB, int RT>
 struct Cfg {
   static constexpr int kConsumers = 8;
   static constexpr int NBS = kConsumers / (HB * RT);      // blocks per stage
-  static constexpr int kThreads = 32 * (kConsumers + 2);  // + KV producer warp + Q producer warp
+  static constexpr int kKvProducers = 2;                  // KV producer warps, alternating stages
+  static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1);  // + Q producer warp
   static constexpr int kSlabs = D / 64;                   // 128-byte swizzle slabs per row
   static constexpr int kHeadTile = 16 * 128;              // one head, 16 rows, one slab
   static constexpr int kBoxBytes = HB * kHeadTile;        // one {64, 16, HB} box
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
 
   const __nv_bfloat16* qglob = static_cast<const __nv_bfloat16*>(p.q);
 
-  if (warp == C::kConsumers + 1) {
+  if (warp == C::kConsumers + C::kKvProducers) {
     // ======================= Q producer =======================
     // Segment by segment, in order, the HB*G query rows of the head box go to a
     // 2-slot ring (in-order issue keeps each parity wait one phase ahead at most).
@@ -252,58 +253,122 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     return;
   }
 
-  if (warp == C::kConsumers) {
-    // ======================= KV producer =======================
-    // One stage at a time: lane 0 claims the ring slot, then the lanes issue the
-    // stage's boxes concurrently.
+  if (warp >= C::kConsumers && warp < C::kConsumers + C::kKvProducers) {
+    // ======================= KV producers =======================
+    // Producer w issues stages w, w + 2, w + 4, ...: lane 0 claims the ring
+    // slot, then the lanes issue the stage's boxes concurrently.  A producer's
+    // serial work per stage caps the rate of small stages (32 KB for MQA), so
+    // two share them, and each keeps its part short: the block_table entries of
+    // its next stage are read while the current one waits for its slot, and the
+    // per-lane box geometry of a full stage is computed once.  (Consumers free
+    // stages in order, so a producer waiting for stage i - S to be freed has
+    // seen stage i - 2 - S freed: it is never two phases ahead of a slot.)
+    const int pw = warp - C::kConsumers;
     const int R = ps < 16 ? ps : 16;  // rows per box (page_size >= 8)
+    // page_size >= 16: one box per (tensor, block) covers every slab; page_size
+    // 8: one box per (tensor, block, slab, 8-row half) so rows land at 16-row pitch
+    const int slabs_per_op = R == 16 ? C::kSlabs : 1;
+    const int boxes_per_block = (16 / R) * (C::kSlabs / slabs_per_op);
+    constexpr int kOpsPerLane = 2;  // at most 2 tensors x 8 blocks x 4 boxes = 64 ops a stage
+    static_assert(2 * NBS * 2 * (D / 64) <= 32 * kOpsPerLane, "ops per stage");
+    // op -> (block jj, first row q*R of the box) and its shared-memory offset in
+    // the stage; tensor TT = K or V, slab sl
+    struct OpGeom {
+      int jj, q, TT, sl;
+      uint32_t off;
+      bool on;
+    };
+    auto geom = [&](int nbs, int op) {
+      OpGeom g;
+      g.on = op < 2 * nbs * boxes_per_block;
+      const int sub = op % boxes_per_block;
+      g.q = sub % (16 / R);
+      g.sl = sub / (16 / R);
+      g.jj = (op / boxes_per_block) % nbs;
+      g.TT = op / (boxes_per_block * nbs);
+      g.off = (uint32_t)(((g.TT * NBS + g.jj) * C::kSlabs + g.sl) * C::kBoxBytes + g.q * R * 128);
+      return g;
+    };
+    // every stage but a segment's last has NBS blocks: its geometry is fixed per lane
+    OpGeom full_geom[kOpsPerLane];
+#pragma unroll
+    for (int x = 0; x < kOpsPerLane; ++x) full_geom[x] = geom(NBS, lane + 32 * x);
+    // raw block_table entries of this lane's ops in the stage at cu (loads only)
+    auto fetch = [&](const Cursor& cu, int nbs, int (&pg)[kOpsPerLane]) {
+      const int32_t* bt = p.block_table + (int64_t)cu.b * p.max_blocks;
+#pragma unroll
+      for (int x = 0; x < kOpsPerLane; ++x) {
+        const OpGeom g = nbs == NBS ? full_geom[x] : geom(nbs, lane + 32 * x);
+        const int kk = (cu.k + g.jj) * 16 + g.q * R;
+        pg[x] = (g.on && nbs > 0 && kk < cu.L) ? __ldg(bt + (kk >> pshift)) : 0;
+      }
+    };
+    // the stage after the one at (c, nb); nb = 0 past the CTA's range
+    auto next_stage = [&](Cursor& c, int& nb) {
+      if (nb == 0) return;
+      advance(c, nb);
+      nb = c.u < u1 ? stage_blocks(c) : 0;
+    };
     Cursor cur = locate(u0);
     bool alive = true;
-    griddep_wait();
-    for (int64_t i = 0; cur.u < u1; ++i) {
-      const int nbs = stage_blocks(cur);
+    int nbs = stage_blocks(cur);
+    int64_t i = 0;
+    if (pw == 1) {
+      next_stage(cur, nbs);
+      i = 1;
+    }
+    // page ids of the current and the next stage; the loop is unrolled by two
+    // with the buffers swapped, so no register holding a load in flight is
+    // ever copied (a copy would wait for the load)
+    int pga[kOpsPerLane], pgb[kOpsPerLane];
+    fetch(cur, nbs, pga);  // block_table is an input, not written by the append kernel
+    griddep_wait();        // the pool rows of this step were written by the append kernel
+    auto stage = [&](int (&pg)[kOpsPerLane], int (&pg_n)[kOpsPerLane]) {
       const int slot = (int)(i % S);
+      Cursor nx = cur;
+      int nbs_n = nbs;
+      next_stage(nx, nbs_n);
+      next_stage(nx, nbs_n);  // this producer's next stage: two ahead
+      fetch(nx, nbs_n, pg_n);
       if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      // page_size >= 16: one box per (tensor, block) covers every slab; page_size
-      // 8: one box per (tensor, block, slab, 8-row half) so rows land at 16-row pitch
-      const int slabs_per_op = R == 16 ? C::kSlabs : 1;
-      const int boxes_per_block = (16 / R) * (C::kSlabs / slabs_per_op);
-      const int nops = 2 * nbs * boxes_per_block;
-      const int32_t* bt = p.block_table + (int64_t)cur.b * p.max_blocks;
       const uint32_t sbase = smem_u32(ring + slot * C::kStageBytes);
-      // op -> (tensor, block, slab, sub-box); -1 row = nothing to load
-      auto op_row = [&](int op, int& sl, int& jj, int& TT, int& q) {
-        const int sub = op % boxes_per_block;
-        q = sub % (16 / R);
-        sl = sub / (16 / R);
-        jj = (op / boxes_per_block) % nbs;
-        TT = op / (boxes_per_block * nbs);
-        const int kk = (cur.k + jj) * 16 + q * R;
-        if (kk >= cur.L) return -1;
-        const int page = __ldg(bt + (kk >> pshift));
-        if (page < 0 || page >= p.pool.num_pages) {
-          if (sl == 0 && TT == 0) record_error(p.err, ERR_BLOCK_TABLE, page);
-          return -1;
-        }
-        return page * ps + (kk & (ps - 1));
-      };
+      int row[kOpsPerLane];
+      uint32_t dst[kOpsPerLane];
       int mine = 0;
-      for (int op = lane; op < nops; op += 32) {
-        int sl, jj, TT, q;
-        mine += op_row(op, sl, jj, TT, q) >= 0;
+#pragma unroll
+      for (int x = 0; x < kOpsPerLane; ++x) {
+        const OpGeom g = nbs == NBS ? full_geom[x] : geom(nbs, lane + 32 * x);
+        const int kk = (cur.k + g.jj) * 16 + g.q * R;
+        row[x] = -1;
+        dst[x] = sbase + g.off;
+        if (g.on && kk < cur.L) {
+          const int page = pg[x];
+          if (page < 0 || page >= p.pool.num_pages) {
+            if (g.sl == 0 && g.TT == 0) record_error(p.err, ERR_BLOCK_TABLE, page);
+          } else {
+            row[x] = page * ps + (kk & (ps - 1));
+            ++mine;
+          }
+        }
       }
       const int issued = __reduce_add_sync(0xffffffffu, mine);
       if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB * slabs_per_op));
       __syncwarp();
-      for (int op = lane; op < nops; op += 32) {
-        int sl, jj, TT, q;
-        const int row = op_row(op, sl, jj, TT, q);
-        if (row < 0) continue;
-        const uint32_t dst = sbase + (uint32_t)(((TT * NBS + jj) * C::kSlabs + sl) * C::kBoxBytes + q * R * 128);
-        tma_load_4d(dst, TT ? &tmap_v : &tmap_k, 0, row, cur.hk * HB, sl, full_bar(slot));
+#pragma unroll
+      for (int x = 0; x < kOpsPerLane; ++x) {
+        if (row[x] < 0) continue;
+        const OpGeom g = nbs == NBS ? full_geom[x] : geom(nbs, lane + 32 * x);
+        tma_load_4d(dst[x], g.TT ? &tmap_v : &tmap_k, 0, row[x], cur.hk * HB, g.sl, full_bar(slot));
       }
-      advance(cur, nbs);
+      cur = nx;
+      nbs = nbs_n;
+      i += C::kKvProducers;
+    };
+    while (nbs > 0) {
+      stage(pga, pgb);
+      if (nbs == 0) break;
+      stage(pgb, pga);
     }
     return;
   }
