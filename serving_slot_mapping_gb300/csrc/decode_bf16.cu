@@ -611,17 +611,32 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   const int64_t seg = (int64_t)b * Hg + hg;
   __nv_bfloat16* outp =
       static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
+  constexpr int kRegParts = 8;  // partial rows held in registers (one load round trip)
   for (int g = warp; g < G; g += 4) {
-    // (m, l) of every partial: lanes stride over the parts
-    float M = -INFINITY;
-    for (int q = lane; q < nparts; q += 32) {
+    // One round trip when nparts <= kRegParts: every lane loads its (m, l) (lane
+    // q = partial q) and its four dims of every partial row at once; the weights
+    // come from the warp max and are broadcast by shuffles.
+    float4 vr[kRegParts];
+    const bool dims = 4 * lane < D;
+#pragma unroll
+    for (int q = 0; q < kRegParts; ++q) {
+      vr[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < nparts && dims && !(some_empty && cta_range_empty(c0 + q, U, n)))
+        vr[q] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D) + lane);
+    }
+    float2 ml_mine = make_float2(-INFINITY, 0.f);  // (m, l) of partial `lane`
+    if (lane < nparts && !(some_empty && cta_range_empty(c0 + lane, U, n)))
+      ml_mine = __ldcg(p.part_ml + ((seg + c0 + lane) * HB + h) * G + g);
+    float M = ml_mine.x;
+    for (int q = lane + 32; q < nparts; q += 32) {
       if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
       M = fmaxf(M, __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g).x);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float den = 0.f;
-    for (int q = lane; q < nparts; q += 32) {
+    const float f_mine = (ml_mine.x == -INFINITY) ? 0.f : fast_exp2(ml_mine.x - M);
+    float den = f_mine * ml_mine.y;
+    for (int q = lane + 32; q < nparts; q += 32) {
       if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
       const float2 ml = __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
       den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
@@ -631,9 +646,16 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
     const float inv = den > 0.f ? 1.f / den : 0.f;
     // weighted sum of the partial rows: lane owns dims 4*lane .. 4*lane+3 (D <= 128)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (4 * lane < D) {
+#pragma unroll
+    for (int q = 0; q < kRegParts; ++q) {
+      const float f = __shfl_sync(0xffffffffu, f_mine, q);
+      if (q < nparts) {
+        acc.x += f * vr[q].x; acc.y += f * vr[q].y; acc.z += f * vr[q].z; acc.w += f * vr[q].w;
+      }
+    }
+    if (dims) {
 #pragma unroll 4
-      for (int q = 0; q < nparts; ++q) {
+      for (int q = kRegParts; q < nparts; ++q) {
         if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
         const int64_t sidx = (seg + c0 + q) * HB + h;
         const float mq = __ldcg(p.part_ml + sidx * G + g).x;
