@@ -20,7 +20,12 @@ What it follows:
   (ROCm/maxtext PR #93 "[Draft] kv paged kernels", the KV-pool sharding
   commit), and an explicit softmax scale (same page, the ``gpu_paged``
   commit and the double-scaling fix);
-* the split-softmax merge identity used to combine partial results.
+* the split-softmax merge identity used to combine partial results;
+* decode over a prefix shared by the whole batch (block tables aliasing the
+  pages of a common prompt prefix: the RadixAttention case of the mobius
+  page, summary, and the prefix index of the maxtext page, M5 commit),
+  defined plainly as attention over the prefix keys followed by the
+  sequence's own keys.
 
 Readings where the pages are silent are listed in the module docstring of
 :mod:`oracle.paged_attention`.
@@ -38,4 +43,5 @@ from .paged_attention import (  # noqa: F401
     paged_attention_decode,
     paged_attention_prefill,
     paged_attention_decode_partial,
+    paged_attention_decode_cascade,
 )

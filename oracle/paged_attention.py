@@ -246,3 +246,33 @@ def paged_attention_prefill(key_pool, value_pool, q, query_start_loc, block_tabl
         pos = [L - n + (r - s0) for r in idx]
         out[idx] = attend(q[idx], K, V, pos, scale)
     return out
+
+
+def paged_attention_decode_cascade(key_pool, value_pool, q, prefix_block_ids, prefix_len,
+                                   block_table, seq_lens, scale, seqs=None):
+    """Decode where every sequence's keys begin with one shared prefix.
+
+    Sequence b attends to the ``prefix_len`` tokens held on the pages
+    ``prefix_block_ids`` -- the same physical pages for every sequence of the
+    batch, as when block tables alias the pages of a shared prompt prefix
+    (the RadixAttention case of mobius PR #395, summary; the page-granular
+    prefix index of ROCm/maxtext PR #93, the prefix cache (M5) commit) --
+    followed by its own ``seq_lens[b]`` tokens on ``block_table[b]``.  The
+    plain definition: gather both page lists, concatenate the keys (and the
+    values), attend with the one decode query.  ``seq_lens`` counts only the
+    sequence's own tokens; a sequence with ``prefix_len + seq_lens[b] = 0``
+    gives 0.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B = q.shape[0]
+    out = np.zeros(q.shape, dtype=np.float64)
+    Kp = gather_pages(key_pool, prefix_block_ids, prefix_len)
+    Vp = gather_pages(value_pool, prefix_block_ids, prefix_len)
+    for b in (range(B) if seqs is None else seqs):
+        L = int(seq_lens[b])
+        K = np.concatenate([Kp, gather_pages(key_pool, block_table[b], L)], axis=0)
+        V = np.concatenate([Vp, gather_pages(value_pool, block_table[b], L)], axis=0)
+        if K.shape[0] == 0:
+            continue
+        out[b] = attend(q[b:b + 1], K, V, [K.shape[0] - 1], scale)[0]
+    return out

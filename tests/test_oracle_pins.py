@@ -432,3 +432,121 @@ def test_tiny_config_decode_after_prefill_oracle_chain():
     assert np.all(np.isfinite(o2))
     # the decode token at position 100 lands in page block_table[6], offset 4
     assert dc.slot_mapping[0] == dc.block_table[0, 6] * 16 + 4
+
+
+# ---------------------------------------------------------------------------
+# cascade decode: a prefix shared by every sequence, then each one's own pages
+# ---------------------------------------------------------------------------
+
+def _cascade_case(rng, prefix_len, lens, hq, hkv, d, ps):
+    """A pool holding one shared prefix and per-sequence suffixes (NaN elsewhere)."""
+    npre = (prefix_len + ps - 1) // ps
+    need = [(L + ps - 1) // ps for L in lens]
+    P = npre + sum(need) + 2
+    perm = rng.permutation(P)
+    kp = np.full((P, ps, hkv, d), np.nan)
+    vp = np.full((P, ps, hkv, d), np.nan)
+    pre_ids = perm[:npre].copy()
+    for j in range(prefix_len):
+        kp[pre_ids[j // ps], j % ps] = _rand(rng, hkv, d)
+        vp[pre_ids[j // ps], j % ps] = _rand(rng, hkv, d)
+    bt = np.full((len(lens), max(max(need), 1)), -1, dtype=np.int64)
+    cur = npre
+    for b, L in enumerate(lens):
+        for m in range(need[b]):
+            bt[b, m] = perm[cur]
+            cur += 1
+        for j in range(L):
+            kp[bt[b, j // ps], j % ps] = _rand(rng, hkv, d)
+            vp[bt[b, j // ps], j % ps] = _rand(rng, hkv, d)
+    return kp, vp, pre_ids, bt
+
+
+def _cascade_brute(kp, vp, q_row, pre_ids, prefix_len, bt_row, L, scale, hkv):
+    """Pure-Python loops: key j < prefix_len at pool[pre_ids[j // ps], j % ps],
+    key prefix_len + i at pool[bt_row[i // ps], i % ps]."""
+    ps = len(kp[0])
+    hq, d = len(q_row), len(q_row[0])
+    G = hq // hkv
+    locs = [(int(pre_ids[j // ps]), j % ps) for j in range(prefix_len)]
+    locs += [(int(bt_row[i // ps]), i % ps) for i in range(L)]
+    out = [[0.0] * d for _ in range(hq)]
+    for h in range(hq):
+        hk = h // G
+        ss = []
+        for page, off in locs:
+            s = 0.0
+            for e in range(d):
+                s += float(q_row[h][e]) * float(kp[page][off][hk][e])
+            ss.append(scale * s)
+        if not ss:
+            continue
+        mx = max(ss)
+        ws = [math.exp(x - mx) for x in ss]
+        tot = sum(ws)
+        for e in range(d):
+            acc = 0.0
+            for w, (page, off) in zip(ws, locs):
+                acc += w * float(vp[page][off][hk][e])
+            out[h][e] = acc / tot
+    return np.array(out)
+
+
+@pytest.mark.parametrize("prefix_len", [0, 5, 8, 13])
+def test_cascade_bruteforce(prefix_len):
+    rng = np.random.RandomState(30 + prefix_len)
+    ps, hq, hkv, d = 4, 4, 2, 6
+    lens = [0, 3, 9]
+    kp, vp, pre_ids, bt = _cascade_case(rng, prefix_len, lens, hq, hkv, d, ps)
+    q = _rand(rng, len(lens), hq, d)
+    got = oracle.paged_attention_decode_cascade(kp, vp, q, pre_ids, prefix_len, bt, lens, 0.45)
+    for b, L in enumerate(lens):
+        exp = _cascade_brute(kp, vp, q[b], pre_ids, prefix_len, bt[b], L, 0.45, hkv)
+        np.testing.assert_allclose(got[b], exp, rtol=1e-12, atol=1e-12)
+
+
+def test_cascade_equals_decode_on_concatenated_tables():
+    """Page-aligned prefix: identical to plain decode over prefix pages ++ own pages."""
+    rng = np.random.RandomState(41)
+    ps, hq, hkv, d = 4, 8, 2, 8
+    prefix_len, lens = 12, [1, 6, 11, 0]
+    kp, vp, pre_ids, bt = _cascade_case(rng, prefix_len, lens, hq, hkv, d, ps)
+    q = _rand(rng, len(lens), hq, d)
+    full = np.concatenate([np.tile(pre_ids, (len(lens), 1)), bt], axis=1)
+    a = oracle.paged_attention_decode_cascade(kp, vp, q, pre_ids, prefix_len, bt, lens, 0.3)
+    c = oracle.paged_attention_decode(kp, vp, q, full, [prefix_len + L for L in lens], 0.3)
+    assert np.array_equal(a, c)
+
+
+def test_cascade_is_merge_of_prefix_and_suffix_partials():
+    """The prefix attended once for all queries, merged with each suffix."""
+    rng = np.random.RandomState(42)
+    ps, hq, hkv, d = 4, 4, 1, 8
+    prefix_len, lens = 10, [7, 2, 0]
+    kp, vp, pre_ids, bt = _cascade_case(rng, prefix_len, lens, hq, hkv, d, ps)
+    q = _rand(rng, len(lens), hq, d) * 2.0
+    Kp = oracle.gather_pages(kp, pre_ids, prefix_len)
+    Vp = oracle.gather_pages(vp, pre_ids, prefix_len)
+    pre = oracle.attend_partial(q, Kp, Vp, [prefix_len - 1] * len(lens), 0.6)
+    suf = oracle.paged_attention_decode_partial(kp, vp, q, bt, lens, 0.6, [(0, L) for L in lens])
+    merged = oracle.merge_partials([pre, suf])
+    whole = oracle.paged_attention_decode_cascade(kp, vp, q, pre_ids, prefix_len, bt, lens, 0.6)
+    np.testing.assert_allclose(merged, whole, rtol=1e-12, atol=1e-13)
+
+
+def test_cascade_degenerate_cases():
+    rng = np.random.RandomState(43)
+    ps, hq, hkv, d = 4, 2, 1, 4
+    kp, vp, pre_ids, bt = _cascade_case(rng, 0, [5, 0], hq, hkv, d, ps)
+    q = _rand(rng, 2, hq, d)
+    # no prefix: plain decode; no prefix and no own tokens: 0
+    a = oracle.paged_attention_decode_cascade(kp, vp, q, pre_ids, 0, bt, [5, 0], 0.5)
+    np.testing.assert_array_equal(a[0], oracle.paged_attention_decode(kp, vp, q, bt, [5, 0], 0.5)[0])
+    assert np.all(a[1] == 0.0)
+    # prefix only (every own length 0): the prefix attention for every query
+    kp, vp, pre_ids, bt = _cascade_case(rng, 6, [0, 0], hq, hkv, d, ps)
+    a = oracle.paged_attention_decode_cascade(kp, vp, q, pre_ids, 6, bt, [0, 0], 0.5)
+    Kp = oracle.gather_pages(kp, pre_ids, 6)
+    Vp = oracle.gather_pages(vp, pre_ids, 6)
+    exp = oracle.attend(q, Kp, Vp, [5, 5], 0.5)
+    np.testing.assert_allclose(a, exp, rtol=1e-13, atol=1e-14)
