@@ -548,6 +548,26 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
                 ub = wl.decode_unique_kv_bytes(plan)
                 ent["unique_kv_GBps"] = round(ub / (ms * 1e-3) / 1e9, 1)
                 ent["unique_frac_hbm"] = round(ub / (ms * 1e-3) / 1e9 / hbm, 4)
+                # the same batch through cascade decode: the shared prefix read once
+                pages = wl.shared_prefix_pages(plan)
+                pre, plen, own_bt, own_lens = wl.cascade_tables(plan, pages, pages * plan.page_size)
+                cw = rig.capi.cascade_workspace(plan.batch, plan.num_q_heads, rig.st.key_pool)
+                pre_t = torch.from_numpy(pre).to(dev)
+                bt_t = torch.from_numpy(own_bt).to(dev)
+                sl_t = torch.from_numpy(own_lens).to(dev)
+                msl = int(own_lens.max())
+
+                def cascade():
+                    rig.capi.paged_attention_decode_cascade(
+                        rig.st.key_pool, rig.st.value_pool, rig.st.q, pre_t, plen, bt_t, sl_t,
+                        plan.scale, max_seq_len=msl, out=rig.out, workspace=cw)
+                gc = capture(cascade, stream)
+                cms = statistics.mean(timed_graph(gc, steps, flush, stream))
+                ent["cascade_ms"] = round(cms, 5)
+                ent["cascade_unique_GBps"] = round(ub / (cms * 1e-3) / 1e9, 1)
+                ent["cascade_unique_frac_hbm"] = round(ub / (cms * 1e-3) / 1e9 / hbm, 4)
+                ent["cascade_tokens_per_s"] = round(plan.batch / (cms * 1e-3), 1)
+                del gc
             res[name] = ent
             del rig, g
             torch.cuda.empty_cache()

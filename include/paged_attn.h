@@ -136,6 +136,47 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode_cascade -- decode for a batch whose sequences all
+ * begin with the same prefix on the same physical pages (block tables that
+ * alias the pages of a common prompt prefix: the RadixAttention case of
+ * mobius PR #395, summary; the page-granular prefix index of ROCm/maxtext
+ * PR #93, prefix cache (M5) commit).  Sequence b attends to
+ *
+ *   the prefix_len tokens on prefix_block_ids, then
+ *   its own seq_lens[b] tokens on block_table[b, ...],
+ *
+ * i.e. exactly paged_attention_decode over the concatenated key lists.  The
+ * prefix is read once for all B query rows (one tensor-core pass with its keys
+ * cut into chunks, fp32 partials) instead of once per sequence; each sequence's
+ * own tokens go through the split-KV decode, and the partials of both are
+ * merged per row.
+ *
+ * prefix_block_ids  device int32 [ceil(prefix_len / page_size)], the shared
+ *                   pages in order (the prefix may end inside its last page).
+ * prefix_len        tokens of the shared prefix, >= 0; 0 runs plain decode.
+ * block_table, seq_lens, max_blocks_per_seq, max_seq_len
+ *                   the sequences' OWN pages and token counts (excluding the
+ *                   prefix); a sequence with seq_lens[b] == 0 attends to the
+ *                   prefix alone.
+ * q, out, scale     as for paged_attention_decode.
+ * workspace         device scratch of at least
+ *                   paged_attention_decode_cascade_workspace_size(...) bytes,
+ *                   16-byte aligned; contents need no initialisation.
+ * bf16 pools only (PA_ERR_UNSUPPORTED for f32), with the bf16 limits of
+ * paged_attention_decode.
+ */
+size_t paged_attention_decode_cascade_workspace_size(int32_t batch, int32_t num_q_heads,
+                                                     int32_t num_kv_heads, int32_t head_dim,
+                                                     int32_t dtype);
+
+pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, void* out,
+                                         int32_t batch, int32_t num_q_heads,
+                                         const int32_t* prefix_block_ids, int32_t prefix_len,
+                                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace.  The pages have no counterpart of this call: it
  * exists for callers that cannot allocate device memory, such as a plugin in

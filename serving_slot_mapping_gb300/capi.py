@@ -48,6 +48,10 @@ SIGNATURES = {
     "paged_attention_decode_static_scratch": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32,
                                                      _c_void_p, _i32, _c_void_p, _i32, _f32,
                                                      _c_void_p]),
+    "paged_attention_decode_cascade_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "paged_attention_decode_cascade": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
+                                              _i32, _c_void_p, _i32, _c_void_p, _i32, _f32,
+                                              _c_void_p, _sz, _c_void_p]),
     "paged_attention_prefill": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i64,
                                        _i32, _c_void_p, _i32, _c_void_p, _i32, _f32, _c_void_p]),
     "paged_device_error": (_i32, [ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -207,6 +211,48 @@ def paged_attention_decode_static_scratch(key_pool, value_pool, q, block_table, 
                                                      int(max_seq_len), float(scale),
                                                      _stream(stream))
     _check(st, "paged_attention_decode_static_scratch")
+    return out
+
+
+def cascade_workspace(batch, num_q_heads, key_pool, device=None) -> Optional[torch.Tensor]:
+    """Allocate (with torch) the scratch buffer paged_attention_decode_cascade needs."""
+    n = int(lib().paged_attention_decode_cascade_workspace_size(
+        batch, num_q_heads, key_pool.shape[2], key_pool.shape[3], _dtype_code(key_pool.dtype)))
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or key_pool.device)
+
+
+def paged_attention_decode_cascade(key_pool, value_pool, q, prefix_block_ids, prefix_len,
+                                   block_table, seq_lens, scale, max_seq_len=None, out=None,
+                                   workspace=None, stream=None):
+    """Decode over a prefix shared by the whole batch, then each sequence's own pages.
+
+    ``prefix_block_ids`` int32 [ceil(prefix_len / page_size)]; ``block_table``
+    int32 [B, max_blocks] and ``seq_lens`` int32 [B] describe each sequence's
+    own tokens only.
+    """
+    pool = make_pool(key_pool, value_pool)
+    _contig(q, "q")
+    _contig(block_table, "block_table")
+    _contig(prefix_block_ids, "prefix_block_ids")
+    B, hq, d = q.shape
+    if (block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32
+            or prefix_block_ids.dtype != torch.int32):
+        raise TypeError("prefix_block_ids, block_table and seq_lens must be int32")
+    mb = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = mb * pool.page_size
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = cascade_workspace(B, hq, key_pool)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_attention_decode_cascade(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
+                                              _ptr(prefix_block_ids), int(prefix_len),
+                                              _ptr(block_table), mb, _ptr(seq_lens), int(max_seq_len),
+                                              float(scale), _ptr(workspace), wbytes, _stream(stream))
+    _check(st, "paged_attention_decode_cascade")
     return out
 
 

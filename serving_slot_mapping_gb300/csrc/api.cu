@@ -173,6 +173,89 @@ size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
   return decode_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, num_sms(), hb);
 }
 
+namespace {
+
+// Launch parameters of the bf16 split-KV decode (shared by plain and cascade
+// decode); the partials take the first bytes of the workspace.
+pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                             int32_t num_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, int32_t max_seq_len, float scale, void* workspace,
+                             size_t workspace_bytes, pa::DecodeParams* p, int reserved_sms = 0) {
+  const int32_t group = num_q_heads / pool->num_kv_heads;
+  if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
+  const int sms = num_sms() - reserved_sms;
+  const int ctas = pa::decode_num_ctas(sms < 1 ? 1 : sms, batch, pool->num_kv_heads, max_seq_len, hb);
+  const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas, hb);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
+  const int budget = max_smem_optin();
+  if (pa::decode_smem_bytes(pool->head_dim, group, batch, hb, budget) > (size_t)budget) return PA_ERR_UNSUPPORTED;
+  const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas, hb);
+  *p = pa::DecodeParams{};
+  p->pool = geom(pool);
+  p->q = q;
+  p->out = out;
+  p->block_table = block_table;
+  p->seq_lens = seq_lens;
+  p->part_o = static_cast<float*>(workspace);
+  const size_t o_bytes = align_up((size_t)(slots * group * pool->head_dim * 4), 256);
+  p->part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
+  p->batch = batch;
+  p->num_q_heads = num_q_heads;
+  p->group = group;
+  p->max_blocks = max_blocks_per_seq;
+  p->num_ctas = ctas;
+  p->heads_per_box = hb;
+  p->smem_budget = budget;
+  p->scale_log2 = (float)((double)scale * kLog2e);
+  p->err = error_word();
+  return PA_OK;
+}
+
+// Cascade decode, prefix pass: key chunks per (row tile, KV head), an upper
+// bound on the chunk count.  The prefix pass runs beside the split kernel
+// (which leaves it the SMs it needs), so it takes about an eighth of the SMs;
+// fewer chunks also mean fewer fp32 partials (B*Hq*D*4 bytes each) for the
+// combine kernel to read back.
+int cascade_chunk_target(int32_t batch, int32_t group, int32_t num_kv_heads) {
+  const int64_t row_ctas = ((int64_t)batch * group + 255) / 256;
+  const int64_t t = num_sms() / (4 * row_ctas * num_kv_heads);
+  return (int)(t < 1 ? 1 : t);
+}
+
+// A second stream per (host thread, device) on which the cascade's prefix pass
+// runs beside the split kernel: forked from and joined back to the caller's
+// stream with events, so the order is kept and stream capture records a fork
+// and a join.  Created on first use (make the first cascade call on a thread
+// before capturing) and kept for the life of the thread.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDev = 64;
+  thread_local SideStream side[kMaxDev];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDev) return nullptr;
+  SideStream& ss = side[dev];
+  if (ss.stream == nullptr) {
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+  }
+  return &ss;
+}
+
+size_t cascade_prefix_bytes(int chunks, int32_t batch, int32_t num_q_heads, int32_t head_dim) {
+  const size_t rows = (size_t)chunks * batch * num_q_heads;
+  return align_up(rows * head_dim * 4, 256) + align_up(rows * 8, 256);
+}
+
+}  // namespace
+
 pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
                                  int32_t num_q_heads, const int32_t* block_table,
                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -205,34 +288,93 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
     p.err = error_word();
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
-  if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
-  const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
-  const int ctas = pa::decode_num_ctas(num_sms(), batch, pool->num_kv_heads, max_seq_len, hb);
-  const size_t need = decode_ws_bytes(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, ctas, hb);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
-  if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
-  const int budget = max_smem_optin();
-  if (pa::decode_smem_bytes(pool->head_dim, group, batch, hb, budget) > (size_t)budget) return PA_ERR_UNSUPPORTED;
-  const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas, hb);
   pa::DecodeParams p;
-  p.pool = g;
-  p.q = q;
-  p.out = out;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.part_o = static_cast<float*>(workspace);
-  const size_t o_bytes = align_up((size_t)(slots * group * pool->head_dim * 4), 256);
-  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
-  p.batch = batch;
-  p.num_q_heads = num_q_heads;
-  p.group = group;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_ctas = ctas;
-  p.heads_per_box = hb;
-  p.smem_budget = budget;
-  p.scale_log2 = (float)((double)scale * kLog2e);
-  p.err = error_word();
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
+                          scale, workspace, workspace_bytes, &p);
+  if (st != PA_OK) return st;
   return pa::launch_decode_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t paged_attention_decode_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                                     int32_t head_dim, int32_t dtype) {
+  if (dtype != PA_DTYPE_BF16) return 0;
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || batch <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+  const int target = cascade_chunk_target(batch, num_q_heads / num_kv_heads, num_kv_heads);
+  return paged_attention_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, dtype) +
+         cascade_prefix_bytes(target, batch, num_q_heads, head_dim);
+}
+
+pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                         int32_t num_q_heads, const int32_t* prefix_block_ids, int32_t prefix_len,
+                                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  pa_status st = check_attention(pool, batch, num_q_heads, max_blocks_per_seq, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (pool->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (prefix_len < 0) return PA_ERR_SHAPE;
+  if (batch == 0) return PA_OK;
+  if (prefix_len == 0)  // nothing shared: plain decode (its workspace is a prefix of this one's)
+    return paged_attention_decode(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens,
+                                  max_seq_len, scale, workspace, workspace_bytes, stream);
+  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      prefix_block_ids == nullptr)
+    return PA_ERR_NULL;
+  if (q == out) return PA_ERR_SHAPE;
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(prefix_block_ids, 4)) return PA_ERR_ALIGN;
+  if ((int64_t)batch * (num_q_heads / pool->num_kv_heads) > INT32_MAX / 2) return PA_ERR_RANGE;
+  if (pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y
+  const int32_t group = num_q_heads / pool->num_kv_heads;
+  const size_t dec_bound =
+      paged_attention_decode_workspace_size(batch, num_q_heads, pool->num_kv_heads, pool->head_dim, PA_DTYPE_BF16);
+  const int target = cascade_chunk_target(batch, group, pool->num_kv_heads);
+  const size_t need = dec_bound + cascade_prefix_bytes(target, batch, num_q_heads, pool->head_dim);
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  // prefix pass: the B decode rows against the shared pages, one set of
+  // partials per key chunk, placed after the decode partials
+  const int nt = (prefix_len + 127) / 128;
+  const int chunk_tiles = (nt + target - 1) / target;
+  const int chunks = (nt + chunk_tiles - 1) / chunk_tiles;
+  const int prefix_ctas = (int)(((int64_t)batch * group + 255) / 256) * pool->num_kv_heads * chunks;
+  pa::DecodeParams p;
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
+                          scale, workspace, dec_bound, &p, prefix_ctas);
+  if (st != PA_OK) return st;
+  float* pre_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + dec_bound);
+  const size_t pre_rows = (size_t)chunks * batch * num_q_heads;
+  float2* pre_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(pre_o) +
+                                             align_up(pre_rows * pool->head_dim * 4, 256));
+  pa::PrefillParams pp{};
+  pp.pool = p.pool;
+  pp.q = q;
+  pp.out = nullptr;
+  pp.block_table = prefix_block_ids;
+  pp.total_q = batch;
+  pp.batch = 1;
+  pp.num_q_heads = num_q_heads;
+  pp.group = group;
+  pp.max_blocks = (prefix_len + pool->page_size - 1) / pool->page_size;
+  pp.max_q_len = batch;
+  pp.scale_log2 = p.scale_log2;
+  pp.err = p.err;
+  pp.part_o = pre_o;
+  pp.part_ml = pre_ml;
+  pp.batch_rows = batch;
+  pp.prefix_len = prefix_len;
+  pp.chunk_tiles = chunk_tiles;
+  p.pre_o = pre_o;
+  p.pre_ml = pre_ml;
+  p.pre_chunks = chunks;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SideStream* side = side_stream();
+  if (side == nullptr) return PA_ERR_CUDA;
+  // fork: the prefix pass starts after everything already queued on s
+  if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (pa::launch_prefill_bf16(pp, side->stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaEventRecord(side->join, side->stream) != cudaSuccess) return PA_ERR_CUDA;
+  // the split kernel runs meanwhile on s; the combine waits for both
+  return pa::launch_decode_cascade_bf16(p, s, side->join) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
@@ -272,7 +414,7 @@ pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* o
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
   if (batch > 65535 || pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y/z limits
-  pa::PrefillParams p;
+  pa::PrefillParams p{};
   p.pool = g;
   p.q = q;
   p.out = out;

@@ -497,7 +497,9 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     la += __shfl_xor_sync(0xffffffffu, la, 2);
     float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
     lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-    const bool complete = (first_k == 0) && (seg_blocks == cc.nblk);
+    // a segment whole in this CTA is finished here, unless a cascade's prefix
+    // partials still have to be merged in (then the combine kernel finishes it)
+    const bool complete = (first_k == 0) && (seg_blocks == cc.nblk) && p.pre_chunks == 0;
     const int64_t seg_id = (int64_t)cc.b * Hg + cc.hk;
     const int64_t pslot = (seg_id + c) * HB + h;  // unique per (segment, CTA, head)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)hk * G) * D;
@@ -600,6 +602,85 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   const int nblk = (seq_len_of(p.seq_lens, b, max_len) + 15) >> 4;
   griddep_wait();
+  if (p.pre_chunks > 0) {
+    // cascade: the pair's own-key partials (none if the sequence has no key of
+    // its own) merged with the shared prefix's partials, one per key chunk
+    const int n = p.num_ctas;
+    int c0 = 0, nparts = 0;
+    bool some_empty = false;
+    int64_t U = 0;
+    if (nblk > 0) {
+      U = total * Hg;
+      const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
+      c0 = cta_of_unit(us, U, n);
+      nparts = cta_of_unit(ue - 1, U, n) - c0 + 1;
+      some_empty = U < n;
+    }
+    const int64_t seg = (int64_t)b * Hg + hg;
+    const int nparts_all = nparts + p.pre_chunks;
+    const int64_t Hq = p.num_q_heads;
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hk * G) * D;
+    for (int g = warp; g < G; g += 4) {
+      const int64_t hq = (int64_t)hk * G + g;
+      auto ml_of = [&](int q) {  // q < nparts: own-key partial q; else prefix chunk q - nparts
+        if (q < nparts) {
+          if (some_empty && cta_range_empty(c0 + q, U, n)) return make_float2(-INFINITY, 0.f);
+          return __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
+        }
+        return __ldcg(p.pre_ml + ((int64_t)(q - nparts) * p.batch + b) * Hq + hq);
+      };
+      auto row_of = [&](int q) {
+        if (q < nparts)
+          return reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D);
+        return reinterpret_cast<const float4*>(p.pre_o + (((int64_t)(q - nparts) * p.batch + b) * Hq + hq) * D);
+      };
+      // (m, l): lane q holds partial q (the first 32), later ones are looped over
+      const float2 ml_mine = lane < nparts_all ? ml_of(lane) : make_float2(-INFINITY, 0.f);
+      float M = ml_mine.x;
+      for (int q = lane + 32; q < nparts_all; q += 32) M = fmaxf(M, ml_of(q).x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f_mine = (ml_mine.x == -INFINITY) ? 0.f : fast_exp2(ml_mine.x - M);
+      float den = f_mine * ml_mine.y;
+      for (int q = lane + 32; q < nparts_all; q += 32) {
+        const float2 ml = ml_of(q);
+        den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      // weighted rows, 8 partials at a time with all their loads in flight; a
+      // partial of weight 0 (empty, or negligible) is not read
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool dims = 4 * lane < D;
+      for (int q0 = 0; q0 < nparts_all; q0 += 8) {
+        float f[8];
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = q0 + u;
+          f[u] = __shfl_sync(0xffffffffu, f_mine, q & 31);
+          if (q >= 32 && q < nparts_all) {
+            const float2 ml = ml_of(q);
+            f[u] = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+          }
+          if (q >= nparts_all) f[u] = 0.f;
+          v[u] = (dims && f[u] != 0.f) ? __ldcg(row_of(q) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc.x += f[u] * v[u].x; acc.y += f[u] * v[u].y; acc.z += f[u] * v[u].z; acc.w += f[u] * v[u].w;
+        }
+      }
+      if (dims) {
+        uint2 packed;
+        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(outp + (int64_t)g * D + 4 * lane) = packed;
+      }
+    }
+    return;
+  }
   if (nblk == 0) return;  // zeroed by the split kernel
   const int64_t U = total * Hg;
   const int n = p.num_ctas;
@@ -746,7 +827,9 @@ size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, 
   return L.stages >= 2 ? (size_t)L.total : (size_t)-1;
 }
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
+namespace {
+
+cudaError_t launch_split_only(const DecodeParams& p, cudaStream_t s) {
   const int D = p.pool.head_dim;
   const int RT = p.group <= 16 ? 1 : 2;
   const int R = p.pool.page_size < 16 ? p.pool.page_size : 16;
@@ -756,9 +839,24 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
   if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs) ||
       !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs))
     return cudaErrorInvalidValue;
-  cudaError_t e = D == 128 ? launch_split_d<128>(p, tk, tv, RT, s) : launch_split_d<64>(p, tk, tv, RT, s);
+  return D == 128 ? launch_split_d<128>(p, tk, tv, RT, s) : launch_split_d<64>(p, tk, tv, RT, s);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
+  cudaError_t e = launch_split_only(p, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, D);
+  return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, p.pool.head_dim);
+}
+
+
+cudaError_t launch_decode_cascade_bf16(const DecodeParams& p, cudaStream_t s, cudaEvent_t prefix_done) {
+  cudaError_t e = launch_split_only(p, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamWaitEvent(s, prefix_done, 0);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, p.pool.head_dim);
 }
 
 }  // namespace pa

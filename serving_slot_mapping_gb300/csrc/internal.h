@@ -50,12 +50,21 @@ struct DecodeParams {
   int32_t num_ctas;       // CTAs of the split kernel (partition count)
   float scale_log2;       // scale * log2(e)
   unsigned long long* err;
+  // cascade decode: the keys of every sequence start with a shared prefix whose
+  // partials (one set per key chunk) are merged in by the combine kernel; the
+  // split kernel then never finalises a row itself.  pre_chunks == 0: plain decode.
+  const float* pre_o;     // [pre_chunks, B, Hq, D] fp32 unnormalised
+  const float2* pre_ml;   // [pre_chunks, B, Hq] (reference max in log2 units, denominator)
+  int32_t pre_chunks;
 };
 // Number of partial slots the split kernel may write for this launch.
 int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size);
 int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box);
 int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t heads_per_box);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
+// Cascade: split kernel on s, then the combine after `prefix_done` (an event
+// recorded once the prefix partials are written) has completed.
+cudaError_t launch_decode_cascade_bf16(const DecodeParams& p, cudaStream_t s, cudaEvent_t prefix_done);
 // Dynamic shared memory the bf16 decode split kernel needs.
 // (size_t)-1 when no stage ring of >= 2 stages fits the budget.
 size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget);
@@ -90,6 +99,16 @@ struct PrefillParams {
   int32_t max_q_len;
   float scale_log2;
   unsigned long long* err;
+  // Shared-prefix pass of cascade decode (part_o != nullptr): one sequence of
+  // prefix_len keys on block_table row 0, queried by the batch's `batch_rows`
+  // decode rows of q [batch_rows, Hq, D], none of them causal; key tiles are
+  // cut into chunks of chunk_tiles (blockIdx.z = chunk) and every chunk writes
+  // unnormalised partials instead of out.
+  float* part_o;          // [chunks, batch_rows, Hq, D] fp32
+  float2* part_ml;        // [chunks, batch_rows, Hq] (reference max in log2 units, denominator)
+  int32_t batch_rows;
+  int32_t prefix_len;
+  int32_t chunk_tiles;
 };
 cudaError_t launch_prefill_bf16(const PrefillParams& p, cudaStream_t s);
 

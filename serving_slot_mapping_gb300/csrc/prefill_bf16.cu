@@ -96,15 +96,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int b = blockIdx.z, hk = blockIdx.y;
+  // shared-prefix pass of cascade decode: one non-causal sequence (the prefix)
+  // queried by every decode row; blockIdx.z is then the key chunk
+  const bool pre = p.part_o != nullptr;
+  const int b = pre ? 0 : blockIdx.z, hk = blockIdx.y;
   const int G = p.group, Hq = p.num_q_heads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int qs = __ldg(p.query_start_loc + b);
-  const int qe = __ldg(p.query_start_loc + b + 1);
+  const int qs = pre ? 0 : __ldg(p.query_start_loc + b);
+  const int qe = pre ? p.batch_rows : __ldg(p.query_start_loc + b + 1);
   const int n = qe - qs;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
   const int max_len = p.max_blocks * ps;
-  int L = __ldg(p.seq_lens + b);
+  int L = pre ? p.prefix_len : __ldg(p.seq_lens + b);
   if (L < 0 || L > max_len) {
     if (tid == 0 && hk == 0 && blockIdx.x == 0) record_error(p.err, ERR_SEQ_LEN, L);
     L = L < 0 ? 0 : max_len;
@@ -118,18 +121,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles = (rows_total + kQT * kBM - 1) / (kQT * kBM);
   const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
   if (tile >= tiles) return;
+  // causal: new token i sits at position first + i; the prefix pass is not
+  // causal (every row sees keys 0..L-1, as a row at position L-1 would)
   const int first = L - n;  // absolute position of new token 0
-  // per query tile t: rows from row0_t, key tiles nt_t with a visible key (0 if the tile has no row)
+  // per query tile t: rows from row0_t, key tiles [jb, nt_t) with a visible key
+  // (nt_t <= jb if the tile has no row)
   int row0_t[kQT], pmin_t[kQT], nt_t[kQT];
 #pragma unroll
   for (int t = 0; t < kQT; ++t) {
     row0_t[t] = (tile * kQT + t) * kBM;
     const int last_row = min(row0_t[t] + kBM, rows_total) - 1;
-    pmin_t[t] = first + row0_t[t] / G;
-    const int pmax = first + last_row / G;
+    pmin_t[t] = pre ? L - 1 : first + row0_t[t] / G;
+    const int pmax = pre ? L - 1 : first + last_row / G;
     nt_t[t] = (row0_t[t] < rows_total && pmax >= 0) ? pmax / kBN + 1 : 0;
   }
-  const int nt = max(nt_t[0], nt_t[1]);  // key tiles the CTA loads
+  // the key tiles this CTA covers: all of them, or one chunk in the prefix pass
+  const int jb = pre ? (int)blockIdx.z * p.chunk_tiles : 0;
+  if (pre) {
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) nt_t[t] = min(nt_t[t], jb + p.chunk_tiles);
+  }
+  const int nt = max(nt_t[0], nt_t[1]);  // end (exclusive) of the key tiles the CTA loads
 
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out);
   const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
@@ -138,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return ((int64_t)(qs + i) * Hq + (int64_t)hk * G + g) * D;
   };
   griddep_launch_dependents();
-  if (nt == 0) {  // no row of this CTA sees any key (invalid input): zeros
+  if (nt <= jb) {  // no row of this CTA sees any key (invalid input): zeros
+    if (pre) return;  // the launch covers every chunk with keys
     griddep_wait();
     const int r0 = row0_t[0];
     for (int idx = tid; idx < kQT * kBM * D; idx += kThreads) {
@@ -213,13 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) t = mbar_test(bar(i >> 1), (uint32_t)(i & 1)) ? 1 : 0;
       return __shfl_sync(0xffffffffu, t, 0) != 0;
     };
-    int jk = 0, jv = 0;
-    int raw = fetch(0);  // block_table is an input, not written by the append kernel
+    int jk = jb, jv = jb;  // next K / V tile to issue (absolute); ring slots count from jb
+    int raw = fetch(jb);  // block_table is an input, not written by the append kernel
     griddep_wait();      // the pool rows of this step were written by the append kernel
     unsigned long long t_last = global_ns();
     while (jv < nt && alive) {
       bool progressed = false;
-      if (jk < nt && (jk < kNSK || slot_free(((B_KEMPTY + jk % kNSK) << 1) | (((jk / kNSK) - 1) & 1)))) {
+      const int jkl = jk - jb, jvl = jv - jb;
+      if (jk < nt && (jkl < kNSK || slot_free(((B_KEMPTY + jkl % kNSK) << 1) | (((jkl / kNSK) - 1) & 1)))) {
         int page = raw;
         if (lane < ops && jk * kBN + lane * kpo < L) {
           if (page < 0 || page >= p.pool.num_pages) {
@@ -230,13 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           page = -1;
         }
         page_ring[(jk & 7) * 32 + lane] = page;
-        issue(&tmap_k, k_base + (jk % kNSK) * C::kKVTile, jk, page, bar(B_KFULL + jk % kNSK));
+        issue(&tmap_k, k_base + (jkl % kNSK) * C::kKVTile, jk, page, bar(B_KFULL + jkl % kNSK));
         ++jk;
         raw = fetch(jk);
         progressed = true;
       }
-      if (jv < jk && (jv < kNSV || slot_free(((B_VEMPTY + jv % kNSV) << 1) | (((jv / kNSV) - 1) & 1)))) {
-        const int s = jv % kNSV;
+      if (jv < jk && (jvl < kNSV || slot_free(((B_VEMPTY + jvl % kNSV) << 1) | (((jvl / kNSV) - 1) & 1)))) {
+        const int s = jvl % kNSV;
         const int page = page_ring[(jv & 7) * 32 + lane];
         const uint32_t vdst = v_base + s * C::kKVTile;
         const int valid = L - jv * kBN;  // keys of this tile below L (>= 1)
@@ -294,9 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (alive) alive = mbar_wait(bar(B_QFULL), 0, p.err);
     const int nt0 = nt_t[0], nt1 = nt_t[1];
     auto issue_s = [&](int t, int j) {
-      const int sk = j % kNSK;
+      const int jl = j - jb;
+      const int sk = jl % kNSK;
       if (t == 0 || j >= nt0) {  // first S of key tile j
-        if (alive) alive = mbar_wait(bar(B_KFULL + sk), (uint32_t)((j / kNSK) & 1), p.err);
+        if (alive) alive = mbar_wait(bar(B_KFULL + sk), (uint32_t)((jl / kNSK) & 1), p.err);
         tc_fence_after();
       }
       const uint64_t qd = q_desc + (uint64_t)((t * C::kQBytes) >> 4);
@@ -310,10 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 1 || j >= nt1) umma_commit(bar(B_KEMPTY + sk));  // last S of key tile j
     };
     auto issue_pv = [&](int t, int j) {
-      const int sv = j % kNSV;
-      if (alive) alive = mbar_wait(bar(B_PFULL + t), (uint32_t)(j & 1), p.err);
+      const int jl = j - jb;
+      const int sv = jl % kNSV;
+      if (alive) alive = mbar_wait(bar(B_PFULL + t), (uint32_t)(jl & 1), p.err);
       if (t == 0 || j >= nt0) {  // first PV of key tile j
-        if (alive) alive = mbar_wait(bar(B_VFULL + sv), (uint32_t)((j / kNSV) & 1), p.err);
+        if (alive) alive = mbar_wait(bar(B_VFULL + sv), (uint32_t)((jl / kNSV) & 1), p.err);
       }
       tc_fence_after();
       const uint64_t vd = v_desc + (uint64_t)((sv * C::kKVTile) >> 4);
@@ -322,13 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)  // O_t += P_t V over 16-key steps (two 8-key blocks each)
         umma_bf16_ts(o_tm, s_tm + kk * 8, vd + (uint64_t)((kk * 2 * C::kRowBlock) >> 4), idesc_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+                     (j > jb || kk > 0) ? 1u : 0u);
       if (j == (t ? nt1 : nt0) - 1) umma_commit(bar(B_ODONE + t));
       if (t == 1 || j >= nt1) umma_commit(bar(B_VEMPTY + sv));  // last PV of key tile j
     };
-    if (nt0 > 0) issue_s(0, 0);
-    if (nt1 > 0) issue_s(1, 0);
-    for (int j = 0; j < nt; ++j) {
+    if (nt0 > jb) issue_s(0, jb);
+    if (nt1 > jb) issue_s(1, jb);
+    for (int j = jb; j < nt; ++j) {
       if (j < nt0) issue_pv(0, j);
       if (j + 1 < nt0) issue_s(0, j + 1);
       if (j < nt1) issue_pv(1, j);
@@ -356,13 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(bar(B_QFULL));
     }
-    const int pos = valid_row ? first + R / G : -1;
+    const int pos = valid_row ? (pre ? L - 1 : first + R / G) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + C::kSCol + t * 128;
     const uint32_t o_col = lane_base + C::kOCol + t * 128;
     float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < ntt; ++j) {
-      if (alive) alive = mbar_wait(bar(B_SFULL + t), (uint32_t)(j & 1), p.err);
+    for (int j = jb; j < ntt; ++j) {
+      if (alive) alive = mbar_wait(bar(B_SFULL + t), (uint32_t)((j - jb) & 1), p.err);
       tc_fence_after();
       const int key0 = j * kBN;
       const bool diag = key0 + kBN - 1 > pmin;  // some key of the tile lies past some row's position
@@ -414,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - tmax);
         m_ref = tmax;
         l *= alpha;
-        rescale = j > 0;
+        rescale = j > jb;
       }
       const float mbase = m_ref == -INFINITY ? 0.f : m_ref;
       // pass 2: P = exp2(x - m) as bf16 pairs, written over the S columns just read
@@ -470,17 +486,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(B_PFULL + t));
     }
     // ---- epilogue: O / l -> bf16 (zeros for a tile that sees no key) ----
-    if (ntt > 0) {
+    const bool has = ntt > jb;
+    if (has) {
       if (alive) alive = mbar_wait(bar(B_ODONE + t), 0, p.err);
       tc_fence_after();
     }
     griddep_wait();  // before the first global write
+    if (pre && has) {
+      // unnormalised partial of this key chunk: O and (reference max, l); the
+      // whole warp takes part in each tcgen05.ld, valid rows store
+      const int64_t pr =
+          valid_row ? ((int64_t)blockIdx.z * n + R / G) * Hq + (int64_t)hk * G + (R - (R / G) * G) : 0;
+      float* po = p.part_o + pr * D;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t o[32];
+        tmem_ld32(o_col + cb * 32, o);
+        tmem_wait_ld();
+        if (valid_row) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(po + cb * 32 + q * 4) =
+                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      if (valid_row) p.part_ml[pr] = make_float2(m_ref, l);
+    }
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = outp + (valid_row ? row_off(R) : 0);
 #pragma unroll
-    for (int cb = 0; cb < D / 32; ++cb) {
+    for (int cb = 0; cb < D / 32 && !pre; ++cb) {
       uint32_t o[32];
-      if (ntt > 0) {
+      if (has) {
         tmem_ld32(o_col + cb * 32, o);
         tmem_wait_ld();
       } else {
@@ -523,7 +560,13 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = ((int64_t)p.max_q_len * p.group + kQT * kBM - 1) / (kQT * kBM);
-  return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, (unsigned)p.batch), dim3(kThreads),
+  unsigned gz = (unsigned)p.batch;
+  if (p.part_o != nullptr) {  // prefix pass of cascade decode: z = key chunk
+    if (p.chunk_tiles <= 0 || p.prefix_len <= 0) return cudaErrorInvalidValue;
+    const int nt = (p.prefix_len + kBN - 1) / kBN;
+    gz = (unsigned)((nt + p.chunk_tiles - 1) / p.chunk_tiles);
+  }
+  return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, gz), dim3(kThreads),
                     (size_t)C::kSmem, s, tk, tv, p);
 }
 

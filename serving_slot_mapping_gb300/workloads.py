@@ -198,6 +198,36 @@ def long_context_plan(hkv=8, batch=256, lo=1024, hi=32768, seed=4, hq=32, d=128,
                              seed, free_frac=0.10)
 
 
+def shared_prefix_pages(plan: StepPlan) -> int:
+    """Number of leading block-table columns that every sequence shares."""
+    bt = plan.block_table
+    n = 0
+    while n < bt.shape[1] and (bt[:, n] == bt[0, n]).all():
+        n += 1
+    return n
+
+
+def cascade_tables(plan: StepPlan, prefix_pages: int, prefix_len: int):
+    """Describe a plan whose sequences all list the same first ``prefix_pages``
+    pages as a cascade decode call: (prefix page ids int32 [prefix_pages],
+    prefix_len, own block table int32 [B, MB - prefix_pages], own token counts
+    int32 [B]).  A sequence's own tokens are those on its pages after the
+    shared ones; slots of the last shared page at or past ``prefix_len`` are
+    not part of the prefix.
+    """
+    bt = plan.block_table
+    B = bt.shape[0]
+    pre = np.ascontiguousarray(bt[0, :prefix_pages]).astype(np.int32)
+    assert prefix_pages == 0 or (bt[:, :prefix_pages] == pre[None, :]).all()
+    assert 0 <= prefix_len <= prefix_pages * plan.page_size
+    own_bt = np.ascontiguousarray(bt[:, prefix_pages:]).astype(np.int32)
+    if own_bt.shape[1] == 0:
+        own_bt = np.full((B, 1), -1, dtype=np.int32)
+    own_lens = (plan.seq_lens.astype(np.int64) - prefix_pages * plan.page_size).astype(np.int32)
+    assert (own_lens >= 0).all()
+    return pre, int(prefix_len), own_bt, own_lens
+
+
 def named_plan(name: str) -> StepPlan:
     table = {
         "gqa_decode": lambda: gqa_decode_plan(),

@@ -107,3 +107,18 @@ def test_prefill_validation(L):
 def test_workspace_size_is_zero_for_f32_and_positive_for_bf16(L):
     assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_F32) == 0
     assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_BF16) > 0
+
+
+def test_cascade_validation(L):
+    f = L.paged_attention_decode_cascade
+    p = _pool()
+    args = lambda **k: dict(dict(q=FAKE, out=ctypes.c_void_p(0x50000), batch=2, hq=32, pre=FAKE, plen=64,
+                                 bt=FAKE, mb=4, sl=FAKE, msl=64, scale=0.1, ws=FAKE, wsb=1 << 30), **k)
+    call = lambda pool, a: f(ctypes.byref(pool), a["q"], a["out"], a["batch"], a["hq"], a["pre"], a["plen"],
+                             a["bt"], a["mb"], a["sl"], a["msl"], a["scale"], a["ws"], a["wsb"], None)
+    assert call(_pool(dtype=capi.PA_DTYPE_F32), args()) == capi.PA_ERR_UNSUPPORTED   # bf16 only
+    assert call(p, args(plen=-1)) == capi.PA_ERR_SHAPE
+    assert call(p, args(pre=None)) == capi.PA_ERR_NULL
+    assert call(p, args(wsb=16)) == capi.PA_ERR_WORKSPACE
+    assert call(p, args(batch=0)) == capi.PA_OK
+    assert L.paged_attention_decode_cascade_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_F32) == 0
