@@ -25,7 +25,10 @@ What it follows:
   pages of a common prompt prefix: the RadixAttention case of the mobius
   page, summary, and the prefix index of the maxtext page, M5 commit),
   defined plainly as attention over the prefix keys followed by the
-  sequence's own keys.
+  sequence's own keys;
+* the compressed (CSR) page-table form ``kv_indptr`` / ``kv_indices`` /
+  ``kv_last_page_len`` named by NVIDIA/recsys-examples PR #400
+  (KVCacheMetadata).
 
 Readings where the pages are silent are listed in the module docstring of
 :mod:`oracle.paged_attention`.
@@ -44,4 +47,7 @@ from .paged_attention import (  # noqa: F401
     paged_attention_prefill,
     paged_attention_decode_partial,
     paged_attention_decode_cascade,
+    csr_pages,
+    paged_attention_decode_csr,
+    paged_attention_prefill_csr,
 )

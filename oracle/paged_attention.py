@@ -276,3 +276,59 @@ def paged_attention_decode_cascade(key_pool, value_pool, q, prefix_block_ids, pr
             continue
         out[b] = attend(q[b:b + 1], K, V, [K.shape[0] - 1], scale)[0]
     return out
+
+
+def csr_pages(kv_indptr, kv_indices, kv_last_page_len, page_size, b):
+    """Sequence b of a CSR page table: (its page ids, its key count).
+
+    The compressed page-table metadata of NVIDIA/recsys-examples PR #400
+    (KVCacheMetadata: kv_indices, kv_indptr, kv_last_page_len), read plainly:
+    the pages are ``kv_indices[kv_indptr[b]:kv_indptr[b+1]]`` in order and the
+    last one holds ``kv_last_page_len[b]`` tokens, so the sequence has
+    ``(n_pages - 1) * page_size + kv_last_page_len[b]`` keys (0 without pages).
+    """
+    lo, hi = int(kv_indptr[b]), int(kv_indptr[b + 1])
+    pages = [int(x) for x in kv_indices[lo:hi]]
+    if not pages:
+        return pages, 0
+    return pages, (len(pages) - 1) * page_size + int(kv_last_page_len[b])
+
+
+def paged_attention_decode_csr(key_pool, value_pool, q, kv_indptr, kv_indices, kv_last_page_len,
+                               scale, seqs=None):
+    """Decode with the page table in CSR form (see :func:`csr_pages`)."""
+    q = np.asarray(q, dtype=np.float64)
+    ps = np.asarray(key_pool).shape[1]
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in (range(q.shape[0]) if seqs is None else seqs):
+        pages, L = csr_pages(kv_indptr, kv_indices, kv_last_page_len, ps, b)
+        if L <= 0:
+            continue
+        K = gather_pages(key_pool, pages, L)
+        V = gather_pages(value_pool, pages, L)
+        out[b] = attend(q[b:b + 1], K, V, [L - 1], scale)[0]
+    return out
+
+
+def paged_attention_prefill_csr(key_pool, value_pool, q, query_start_loc, kv_indptr, kv_indices,
+                                kv_last_page_len, scale, rows=None):
+    """Varlen causal prefill with the page table in CSR form (see
+    :func:`csr_pages` and :func:`paged_attention_prefill`)."""
+    q = np.asarray(q, dtype=np.float64)
+    ps = np.asarray(key_pool).shape[1]
+    out = np.zeros(q.shape, dtype=np.float64)
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    want = None if rows is None else set(int(r) for r in rows)
+    for b in range(qsl.shape[0] - 1):
+        s0, s1 = int(qsl[b]), int(qsl[b + 1])
+        n = s1 - s0
+        idx = list(range(s0, s1)) if want is None else [r for r in range(s0, s1) if r in want]
+        if n <= 0 or not idx:
+            continue
+        pages, L = csr_pages(kv_indptr, kv_indices, kv_last_page_len, ps, b)
+        if L <= 0:
+            continue
+        K = gather_pages(key_pool, pages, L)
+        V = gather_pages(value_pool, pages, L)
+        out[idx] = attend(q[idx], K, V, [L - n + (r - s0) for r in idx], scale)
+    return out

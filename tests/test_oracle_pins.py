@@ -550,3 +550,64 @@ def test_cascade_degenerate_cases():
     Vp = oracle.gather_pages(vp, pre_ids, 6)
     exp = oracle.attend(q, Kp, Vp, [5, 5], 0.5)
     np.testing.assert_allclose(a, exp, rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# CSR page tables (kv_indptr / kv_indices / kv_last_page_len)
+# ---------------------------------------------------------------------------
+
+def _to_csr(bt, lens, ps):
+    """Dense block-table rows -> (kv_indptr, kv_indices, kv_last_page_len), by hand."""
+    indptr, indices, last = [0], [], []
+    for b, L in enumerate(lens):
+        n = (L + ps - 1) // ps
+        indices.extend(int(x) for x in bt[b, :n])
+        indptr.append(len(indices))
+        last.append(L - (n - 1) * ps if n else 0)
+    return np.array(indptr), np.array(indices, dtype=np.int64), np.array(last)
+
+
+def test_csr_decode_bruteforce_and_dense_equivalence():
+    rng = np.random.RandomState(50)
+    ps, hq, hkv, d = 4, 4, 2, 6
+    lens = [1, 4, 9, 0, 16]                 # full last pages, a partial one, an empty sequence
+    kp, vp, bt, DK, DV = _paged_case(rng, lens, hq, hkv, d, ps)
+    ip, ix, last = _to_csr(bt, lens, ps)
+    q = _rand(rng, len(lens), hq, d)
+    got = oracle.paged_attention_decode_csr(kp, vp, q, ip, ix, last, 0.41)
+    for b, L in enumerate(lens):
+        pages, LL = oracle.csr_pages(ip, ix, last, ps, b)
+        assert LL == L                      # the key count the tokens laid down define
+        exp = _attn_brute(kp, vp, q[b:b + 1], bt[b], L, 1, 0.41, hkv)[0] if L else np.zeros((hq, d))
+        np.testing.assert_allclose(got[b], exp, rtol=1e-12, atol=1e-12)
+    dense = oracle.paged_attention_decode(kp, vp, q, bt, lens, 0.41)
+    assert np.array_equal(got, dense)
+
+
+def test_csr_prefill_equals_dense_sdpa():
+    rng = np.random.RandomState(51)
+    ps, hq, hkv, d = 8, 8, 2, 16
+    cached, new = [0, 17, 40], [9, 30, 1]
+    lens = [c + n for c, n in zip(cached, new)]
+    kp, vp, bt, DK, DV = _paged_case(rng, lens, hq, hkv, d, ps)
+    ip, ix, last = _to_csr(bt, lens, ps)
+    qsl = np.concatenate([[0], np.cumsum(new)])
+    q = _rand(rng, int(qsl[-1]), hq, d)
+    got = oracle.paged_attention_prefill_csr(kp, vp, q, qsl, ip, ix, last, 0.33)
+    for b in range(len(lens)):
+        exp = _sdpa_dense(q[qsl[b]:qsl[b + 1]], DK[b], DV[b], new[b], 0.33)
+        np.testing.assert_allclose(got[qsl[b]:qsl[b + 1]], exp, rtol=1e-10, atol=1e-12)
+
+
+def test_csr_shared_pages_between_sequences():
+    """Two sequences whose CSR slices list the same physical pages read the same keys."""
+    rng = np.random.RandomState(52)
+    ps, hq, hkv, d = 4, 2, 1, 4
+    kp = _rand(rng, 6, ps, hkv, d)
+    vp = _rand(rng, 6, ps, hkv, d)
+    ip = np.array([0, 3, 6])
+    ix = np.array([2, 0, 5, 2, 0, 5])
+    last = np.array([3, 3])
+    q = np.repeat(_rand(rng, 1, hq, d), 2, axis=0)
+    out = oracle.paged_attention_decode_csr(kp, vp, q, ip, ix, last, 0.5)
+    assert np.array_equal(out[0], out[1])
