@@ -136,6 +136,46 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * CSR page tables.  paged_attention_decode_csr / paged_attention_prefill_csr
+ * are paged_attention_decode / paged_attention_prefill with each sequence's
+ * pages given in the compressed form of NVIDIA/recsys-examples PR #400
+ * (KVCacheMetadata: kv_indices, kv_indptr, kv_last_page_len) instead of a
+ * row-padded block_table and seq_lens:
+ *
+ *   pages of sequence b = kv_indices[kv_indptr[b] .. kv_indptr[b+1]),
+ *   L_b = (kv_indptr[b+1] - kv_indptr[b] - 1) * page_size + kv_last_page_len[b]
+ *         (0 when the sequence has no page),
+ *
+ * i.e. the last page holds kv_last_page_len[b] tokens, 1 .. page_size.
+ *
+ * kv_indptr         device int32 [batch + 1], non-decreasing, kv_indptr[0] >= 0,
+ *                   kv_indptr[batch] <= num_kv_indices.
+ * kv_indices        device int32 [num_kv_indices], physical page ids.
+ * kv_last_page_len  device int32 [batch].
+ * max_seq_len       host upper bound of every L_b.
+ * Device contents the host cannot check: a slice of kv_indptr outside
+ * [0, num_kv_indices] or running backwards is treated as an empty sequence and
+ * a kv_last_page_len outside [1, page_size] is clamped; both are recorded in
+ * the device error word (code 3, see paged_device_error).  Every other argument, and the
+ * workspace of the decode call (paged_attention_decode_workspace_size), is as
+ * for the row-padded calls.
+ */
+pa_status paged_attention_decode_csr(const pa_kv_pool* pool, const void* q, void* out,
+                                     int32_t batch, int32_t num_q_heads,
+                                     const int32_t* kv_indptr, const int32_t* kv_indices,
+                                     int64_t num_kv_indices, const int32_t* kv_last_page_len,
+                                     int32_t max_seq_len, float scale, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+pa_status paged_attention_prefill_csr(const pa_kv_pool* pool, const void* q, void* out,
+                                      int32_t batch, int32_t num_q_heads,
+                                      const int32_t* query_start_loc, int64_t total_q,
+                                      int32_t max_q_len, const int32_t* kv_indptr,
+                                      const int32_t* kv_indices, int64_t num_kv_indices,
+                                      const int32_t* kv_last_page_len, int32_t max_seq_len,
+                                      float scale, void* stream);
+
+/*
  * paged_attention_decode_cascade -- decode for a batch whose sequences all
  * begin with the same prefix on the same physical pages (block tables that
  * alias the pages of a common prompt prefix: the RadixAttention case of
@@ -241,9 +281,10 @@ pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* o
 /*
  * paged_device_error -- read and clear the device error word of the current
  * device.  Synchronises the device.  *code = 0 when no violation was seen,
- * else 1 = block_table entry out of range, 2 = slot out of range,
- * 3 = seq_len out of range, 4 = query_start_loc inconsistent; *detail holds
- * the offending value.  Either pointer may be NULL.
+ * else 1 = block_table / kv_indices entry out of range, 2 = slot out of
+ * range, 3 = seq_len (or CSR kv_indptr / kv_last_page_len) out of range,
+ * 4 = query_start_loc inconsistent, 5 = a bounded wait inside a kernel gave
+ * up; *detail holds the offending value.  Either pointer may be NULL.
  */
 pa_status paged_device_error(int64_t* code, int64_t* detail);
 

@@ -52,6 +52,12 @@ SIGNATURES = {
     "paged_attention_decode_cascade": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
                                               _i32, _c_void_p, _i32, _c_void_p, _i32, _f32,
                                               _c_void_p, _sz, _c_void_p]),
+    "paged_attention_decode_csr": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
+                                          _c_void_p, _i64, _c_void_p, _i32, _f32, _c_void_p, _sz,
+                                          _c_void_p]),
+    "paged_attention_prefill_csr": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i64,
+                                           _i32, _c_void_p, _c_void_p, _i64, _c_void_p, _i32, _f32,
+                                           _c_void_p]),
     "paged_attention_prefill": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i64,
                                        _i32, _c_void_p, _i32, _c_void_p, _i32, _f32, _c_void_p]),
     "paged_device_error": (_i32, [ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -288,3 +294,51 @@ def device_error():
     code, detail = _i64(0), _i64(0)
     _check(lib().paged_device_error(ctypes.byref(code), ctypes.byref(detail)), "paged_device_error")
     return int(code.value), int(detail.value)
+
+
+def _csr_args(kv_indptr, kv_indices, kv_last_page_len):
+    for name, t in (("kv_indptr", kv_indptr), ("kv_indices", kv_indices),
+                    ("kv_last_page_len", kv_last_page_len)):
+        _contig(t, name)
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    return _ptr(kv_indptr), _ptr(kv_indices), int(kv_indices.numel()), _ptr(kv_last_page_len)
+
+
+def paged_attention_decode_csr(key_pool, value_pool, q, kv_indptr, kv_indices, kv_last_page_len,
+                               scale, max_seq_len, out=None, workspace=None, stream=None):
+    """Decode with the page table in CSR form: sequence b's pages are
+    ``kv_indices[kv_indptr[b]:kv_indptr[b+1]]``, its last page holds
+    ``kv_last_page_len[b]`` tokens (all int32 device tensors)."""
+    pool = make_pool(key_pool, value_pool)
+    _contig(q, "q")
+    B, hq, d = q.shape
+    ip, ix, nix, last = _csr_args(kv_indptr, kv_indices, kv_last_page_len)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, key_pool)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_attention_decode_csr(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq, ip, ix, nix, last,
+                                          int(max_seq_len), float(scale), _ptr(workspace), wbytes,
+                                          _stream(stream))
+    _check(st, "paged_attention_decode_csr")
+    return out
+
+
+def paged_attention_prefill_csr(key_pool, value_pool, q, query_start_loc, kv_indptr, kv_indices,
+                                kv_last_page_len, scale, max_q_len, max_seq_len, out=None, stream=None):
+    """Varlen causal prefill with the page table in CSR form."""
+    pool = make_pool(key_pool, value_pool)
+    _contig(q, "q")
+    _contig(query_start_loc, "query_start_loc")
+    T, hq, d = q.shape
+    B = query_start_loc.numel() - 1
+    ip, ix, nix, last = _csr_args(kv_indptr, kv_indices, kv_last_page_len)
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib().paged_attention_prefill_csr(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
+                                           _ptr(query_start_loc), T, int(max_q_len), ip, ix, nix, last,
+                                           int(max_seq_len), float(scale), _stream(stream))
+    _check(st, "paged_attention_prefill_csr")
+    return out

@@ -175,11 +175,40 @@ size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
 
 namespace {
 
+// Host view of the page-table arguments: the dense form (block_table rows +
+// seq_lens) or the CSR form (kv_indptr slices of kv_indices +
+// kv_last_page_len); the kernels read either through page_list_start /
+// seq_keys.
+struct Table {
+  const int32_t* ids = nullptr;       // block_table, or kv_indices
+  const int32_t* seq_lens = nullptr;  // dense
+  const int32_t* indptr = nullptr;    // CSR
+  const int32_t* last = nullptr;      // CSR
+  int64_t kv_len = 0;                 // CSR: entries of kv_indices
+  int32_t max_blocks = 0;             // dense row length (CSR: ceil(max_seq_len / page_size))
+};
+
+pa_status check_table(const Table& t) {
+  if (t.ids == nullptr) return PA_ERR_NULL;
+  if (t.indptr == nullptr ? t.seq_lens == nullptr : t.last == nullptr) return PA_ERR_NULL;
+  if (!aligned(t.ids, 4) || !aligned(t.seq_lens, 4) || !aligned(t.indptr, 4) || !aligned(t.last, 4))
+    return PA_ERR_ALIGN;
+  if (t.indptr != nullptr && t.kv_len < 0) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+Table dense_table(const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens) {
+  Table t;
+  t.ids = block_table;
+  t.seq_lens = seq_lens;
+  t.max_blocks = max_blocks;
+  return t;
+}
+
 // Launch parameters of the bf16 split-KV decode (shared by plain and cascade
 // decode); the partials take the first bytes of the workspace.
 pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
-                             int32_t num_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,
-                             const int32_t* seq_lens, int32_t max_seq_len, float scale, void* workspace,
+                             int32_t num_q_heads, const Table& t, int32_t max_seq_len, float scale, void* workspace,
                              size_t workspace_bytes, pa::DecodeParams* p, int reserved_sms = 0) {
   const int32_t group = num_q_heads / pool->num_kv_heads;
   if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
@@ -196,15 +225,18 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   p->pool = geom(pool);
   p->q = q;
   p->out = out;
-  p->block_table = block_table;
-  p->seq_lens = seq_lens;
+  p->block_table = t.ids;
+  p->seq_lens = t.seq_lens;
+  p->kv_indptr = t.indptr;
+  p->kv_last_page_len = t.last;
+  p->kv_len = t.kv_len;
   p->part_o = static_cast<float*>(workspace);
   const size_t o_bytes = align_up((size_t)(slots * group * pool->head_dim * 4), 256);
   p->part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
   p->batch = batch;
   p->num_q_heads = num_q_heads;
   p->group = group;
-  p->max_blocks = max_blocks_per_seq;
+  p->max_blocks = t.max_blocks;
   p->num_ctas = ctas;
   p->heads_per_box = hb;
   p->smem_budget = budget;
@@ -256,43 +288,141 @@ size_t cascade_prefix_bytes(int chunks, int32_t batch, int32_t num_q_heads, int3
 
 }  // namespace
 
-pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
-                                 int32_t num_q_heads, const int32_t* block_table,
-                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                 int32_t max_seq_len, float scale, void* workspace,
-                                 size_t workspace_bytes, void* stream) {
-  pa_status st = check_attention(pool, batch, num_q_heads, max_blocks_per_seq, max_seq_len, scale);
+namespace {
+
+pa_status decode_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t batch, int32_t num_q_heads,
+                      const Table& t, int32_t max_seq_len, float scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
   if (st != PA_OK) return st;
   if (batch == 0) return PA_OK;
-  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr) return PA_ERR_NULL;
+  if (q == nullptr || out == nullptr) return PA_ERR_NULL;
+  st = check_table(t);
+  if (st != PA_OK) return st;
   if (q == out) return PA_ERR_SHAPE;
-  if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return PA_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const pa::PoolGeom g = geom(pool);
-  const int32_t group = num_q_heads / pool->num_kv_heads;
   if (pool->dtype == PA_DTYPE_F32) {
     if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
-    pa::AttnF32Params p;
-    p.pool = g;
+    pa::AttnF32Params p{};
+    p.pool = geom(pool);
     p.q = static_cast<const float*>(q);
     p.out = static_cast<float*>(out);
     p.query_start_loc = nullptr;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
+    p.block_table = t.ids;
+    p.seq_lens = t.seq_lens;
+    p.kv_indptr = t.indptr;
+    p.kv_last_page_len = t.last;
+    p.kv_len = t.kv_len;
     p.rows = batch;
     p.batch = batch;
     p.num_q_heads = num_q_heads;
-    p.group = group;
-    p.max_blocks = max_blocks_per_seq;
+    p.group = num_q_heads / pool->num_kv_heads;
+    p.max_blocks = t.max_blocks;
     p.scale = scale;
     p.err = error_word();
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
   pa::DecodeParams p;
-  st = bf16_decode_params(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
-                          scale, workspace, workspace_bytes, &p);
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, &p);
   if (st != PA_OK) return st;
   return pa::launch_decode_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t batch, int32_t num_q_heads,
+                       const int32_t* query_start_loc, int64_t total_q, int32_t max_q_len, const Table& t,
+                       int32_t max_seq_len, float scale, void* stream) {
+  pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (total_q < 0 || max_q_len < 0 || total_q > INT32_MAX) return PA_ERR_SHAPE;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  if (max_q_len == 0) return PA_ERR_SHAPE;
+  if (q == nullptr || out == nullptr || query_start_loc == nullptr) return PA_ERR_NULL;
+  st = check_table(t);
+  if (st != PA_OK) return st;
+  if (q == out) return PA_ERR_SHAPE;
+  if (!aligned(query_start_loc, 4)) return PA_ERR_ALIGN;
+  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const pa::PoolGeom g = geom(pool);
+  const int32_t group = num_q_heads / pool->num_kv_heads;
+  if (pool->dtype == PA_DTYPE_F32) {
+    pa::AttnF32Params p{};
+    p.pool = g;
+    p.q = static_cast<const float*>(q);
+    p.out = static_cast<float*>(out);
+    p.query_start_loc = query_start_loc;
+    p.block_table = t.ids;
+    p.seq_lens = t.seq_lens;
+    p.kv_indptr = t.indptr;
+    p.kv_last_page_len = t.last;
+    p.kv_len = t.kv_len;
+    p.rows = total_q;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.max_blocks = t.max_blocks;
+    p.scale = scale;
+    p.err = error_word();
+    return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
+  if (batch > 65535 || pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y/z limits
+  pa::PrefillParams p{};
+  p.pool = g;
+  p.q = q;
+  p.out = out;
+  p.query_start_loc = query_start_loc;
+  p.block_table = t.ids;
+  p.seq_lens = t.seq_lens;
+  p.kv_indptr = t.indptr;
+  p.kv_last_page_len = t.last;
+  p.kv_len = t.kv_len;
+  p.total_q = total_q;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.group = group;
+  p.max_blocks = t.max_blocks;
+  p.max_q_len = max_q_len;
+  p.scale_log2 = (float)((double)scale * kLog2e);
+  p.err = error_word();
+  return pa::launch_prefill_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// The CSR form as a Table; max_seq_len bounds every sequence's keys.
+pa_status csr_table(const pa_kv_pool* pool, const int32_t* kv_indptr, const int32_t* kv_indices, int64_t kv_len,
+                    const int32_t* kv_last_page_len, int32_t max_seq_len, Table* t) {
+  if (pool == nullptr || pool->page_size <= 0) return PA_ERR_NULL;
+  if (kv_indptr == nullptr) return PA_ERR_NULL;
+  if (max_seq_len < 0 || kv_len < 0) return PA_ERR_SHAPE;
+  *t = Table{};
+  t->ids = kv_indices;
+  t->indptr = kv_indptr;
+  t->last = kv_last_page_len;
+  t->kv_len = kv_len;
+  const int64_t mb = ((int64_t)max_seq_len + pool->page_size - 1) / pool->page_size;
+  t->max_blocks = (int32_t)(mb < 1 ? 1 : mb);
+  return PA_OK;
+}
+
+}  // namespace
+
+pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                 int32_t num_q_heads, const int32_t* block_table,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float scale, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return decode_impl(pool, q, out, batch, num_q_heads, dense_table(block_table, max_blocks_per_seq, seq_lens),
+                     max_seq_len, scale, workspace, workspace_bytes, stream);
+}
+
+pa_status paged_attention_decode_csr(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                     int32_t num_q_heads, const int32_t* kv_indptr, const int32_t* kv_indices,
+                                     int64_t num_kv_indices, const int32_t* kv_last_page_len,
+                                     int32_t max_seq_len, float scale, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  Table t;
+  const pa_status st = csr_table(pool, kv_indptr, kv_indices, num_kv_indices, kv_last_page_len, max_seq_len, &t);
+  if (st != PA_OK) return st;
+  return decode_impl(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, stream);
 }
 
 size_t paged_attention_decode_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -337,8 +467,8 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
   const int chunks = (nt + chunk_tiles - 1) / chunk_tiles;
   const int prefix_ctas = (int)(((int64_t)batch * group + 255) / 256) * pool->num_kv_heads * chunks;
   pa::DecodeParams p;
-  st = bf16_decode_params(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens, max_seq_len,
-                          scale, workspace, dec_bound, &p, prefix_ctas);
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, dense_table(block_table, max_blocks_per_seq, seq_lens),
+                          max_seq_len, scale, workspace, dec_bound, &p, prefix_ctas);
   if (st != PA_OK) return st;
   float* pre_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + dec_bound);
   const size_t pre_rows = (size_t)chunks * batch * num_q_heads;
@@ -382,54 +512,20 @@ pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* o
                                   int32_t max_q_len, const int32_t* block_table,
                                   int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                   int32_t max_seq_len, float scale, void* stream) {
-  pa_status st = check_attention(pool, batch, num_q_heads, max_blocks_per_seq, max_seq_len, scale);
+  return prefill_impl(pool, q, out, batch, num_q_heads, query_start_loc, total_q, max_q_len,
+                      dense_table(block_table, max_blocks_per_seq, seq_lens), max_seq_len, scale, stream);
+}
+
+pa_status paged_attention_prefill_csr(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                      int32_t num_q_heads, const int32_t* query_start_loc, int64_t total_q,
+                                      int32_t max_q_len, const int32_t* kv_indptr, const int32_t* kv_indices,
+                                      int64_t num_kv_indices, const int32_t* kv_last_page_len,
+                                      int32_t max_seq_len, float scale, void* stream) {
+  Table t;
+  const pa_status st = csr_table(pool, kv_indptr, kv_indices, num_kv_indices, kv_last_page_len, max_seq_len, &t);
   if (st != PA_OK) return st;
-  if (total_q < 0 || max_q_len < 0 || total_q > INT32_MAX) return PA_ERR_SHAPE;
-  if (batch == 0 || total_q == 0) return PA_OK;
-  if (max_q_len == 0) return PA_ERR_SHAPE;
-  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr ||
-      query_start_loc == nullptr)
-    return PA_ERR_NULL;
-  if (q == out) return PA_ERR_SHAPE;
-  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4)) return PA_ERR_ALIGN;
-  if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const pa::PoolGeom g = geom(pool);
-  const int32_t group = num_q_heads / pool->num_kv_heads;
-  if (pool->dtype == PA_DTYPE_F32) {
-    pa::AttnF32Params p;
-    p.pool = g;
-    p.q = static_cast<const float*>(q);
-    p.out = static_cast<float*>(out);
-    p.query_start_loc = query_start_loc;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.rows = total_q;
-    p.batch = batch;
-    p.num_q_heads = num_q_heads;
-    p.group = group;
-    p.max_blocks = max_blocks_per_seq;
-    p.scale = scale;
-    p.err = error_word();
-    return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-  }
-  if (batch > 65535 || pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y/z limits
-  pa::PrefillParams p{};
-  p.pool = g;
-  p.q = q;
-  p.out = out;
-  p.query_start_loc = query_start_loc;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.total_q = total_q;
-  p.batch = batch;
-  p.num_q_heads = num_q_heads;
-  p.group = group;
-  p.max_blocks = max_blocks_per_seq;
-  p.max_q_len = max_q_len;
-  p.scale_log2 = (float)((double)scale * kLog2e);
-  p.err = error_word();
-  return pa::launch_prefill_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return prefill_impl(pool, q, out, batch, num_q_heads, query_start_loc, total_q, max_q_len, t, max_seq_len, scale,
+                      stream);
 }
 
 pa_status paged_device_error(int64_t* code, int64_t* detail) {

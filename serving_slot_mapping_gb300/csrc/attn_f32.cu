@@ -46,11 +46,7 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(AttnF32Params p) {
       n = __ldg(p.query_start_loc + b + 1) - s0;
       i = (int)(r - s0);
     }
-    int L = __ldg(p.seq_lens + b);
-    if (L < 0 || L > max_len) {
-      if (lane == 0) record_error(p.err, ERR_SEQ_LEN, L);
-      L = L < 0 ? 0 : max_len;
-    }
+    const int L = seq_keys(p.seq_lens, p.kv_indptr, p.kv_last_page_len, p.kv_len, b, ps, max_len, lane == 0 ? p.err : nullptr);
     const int pos = L - n + i;
     const float* qrow = p.q + (r * Hq + h) * (int64_t)D;
     float qv[kMaxPerLane], ov[kMaxPerLane];
@@ -61,7 +57,7 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(AttnF32Params p) {
       ov[t] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
+    const int32_t* bt = p.block_table + page_list_start(p.kv_indptr, p.max_blocks, b);
     for (int j = 0; j <= pos; ++j) {
       const int page = __ldg(bt + j / ps);
       if (page < 0 || page >= p.pool.num_pages) {

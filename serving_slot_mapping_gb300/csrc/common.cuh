@@ -75,6 +75,51 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ---- page tables --------------------------------------------------------------
+// A sequence's pages come from one of two forms:
+//  * dense: a row-padded block_table [B, max_blocks] and seq_lens [B];
+//  * CSR:   kv_indptr [B+1] into kv_indices (passed as block_table) and
+//           kv_last_page_len [B]: sequence b's pages are
+//           kv_indices[kv_indptr[b] .. kv_indptr[b+1]) and its last page holds
+//           kv_last_page_len[b] tokens (the page-table metadata of
+//           NVIDIA/recsys-examples PR #400, KVCacheMetadata), so it has
+//           (n_pages - 1) * page_size + kv_last_page_len[b] keys.
+// Offset of sequence b's first entry in block_table / kv_indices.
+__device__ __forceinline__ int64_t page_list_start(const int32_t* kv_indptr, int max_blocks, int b) {
+  return kv_indptr != nullptr ? (int64_t)__ldg(kv_indptr + b) : (int64_t)b * max_blocks;
+}
+
+// Keys of sequence b.  Dense: seq_lens[b], clamped to [0, max_len].  CSR: from
+// the page count and the last page's fill, which is clamped to [1, page_size];
+// a slice of kv_indptr outside [0, kv_len] or running backwards counts as no
+// page (so nothing past kv_indices is ever read).  Out-of-range inputs are
+// recorded when err is given.
+__device__ __forceinline__ int seq_keys(const int32_t* seq_lens, const int32_t* kv_indptr,
+                                        const int32_t* kv_last_page_len, int64_t kv_len, int b, int page_size,
+                                        int max_len, unsigned long long* err) {
+  if (kv_indptr == nullptr) {
+    int L = __ldg(seq_lens + b);
+    if (L < 0 || L > max_len) {
+      if (err != nullptr) record_error(err, ERR_SEQ_LEN, L);
+      L = L < 0 ? 0 : max_len;
+    }
+    return L;
+  }
+  const int s0 = __ldg(kv_indptr + b), s1 = __ldg(kv_indptr + b + 1);
+  if (s0 < 0 || s1 < s0 || (int64_t)s1 > kv_len) {
+    if (err != nullptr) record_error(err, ERR_SEQ_LEN, s1);
+    return 0;
+  }
+  const int n = s1 - s0;
+  if (n == 0) return 0;
+  int last = __ldg(kv_last_page_len + b);
+  if (last < 1 || last > page_size) {
+    if (err != nullptr) record_error(err, ERR_SEQ_LEN, last);
+    last = last < 1 ? 1 : page_size;
+  }
+  return (n - 1) * page_size + last;
+}
+
 // 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32):
 // results below 2^-126 flush to zero, which changes no attention weight that
 // survives the bf16 / fp32 sums.

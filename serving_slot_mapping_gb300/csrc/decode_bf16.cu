@@ -47,19 +47,13 @@ namespace pa {
 
 namespace {
 
-__device__ __forceinline__ int nblk_of(const int32_t* seq_lens, int b, int max_len,
-                                       unsigned long long* err) {
-  int L = __ldg(seq_lens + b);
-  if (L < 0 || L > max_len) {
-    record_error(err, ERR_SEQ_LEN, L);
-    L = L < 0 ? 0 : max_len;
-  }
-  return (L + 15) >> 4;
+// keys of sequence b (either page-table form), with / without recording bad input
+__device__ __forceinline__ int nblk_of(const DecodeParams& p, int b, int max_len) {
+  return (seq_keys(p.seq_lens, p.kv_indptr, p.kv_last_page_len, p.kv_len, b, p.pool.page_size, max_len, p.err) + 15) >> 4;
 }
 
-__device__ __forceinline__ int seq_len_of(const int32_t* seq_lens, int b, int max_len) {
-  int L = __ldg(seq_lens + b);
-  return L < 0 ? 0 : (L > max_len ? max_len : L);
+__device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b, int max_len) {
+  return seq_keys(p.seq_lens, p.kv_indptr, p.kv_last_page_len, p.kv_len, b, p.pool.page_size, max_len, nullptr);
 }
 
 // CTA that owns unit u when U units are cut into n ranges [c*U/n, (c+1)*U/n).
@@ -156,7 +150,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     }
     fence_mbar_init();
   }
-  for (int b = tid; b < B; b += C::kThreads) prefix[b + 1] = nblk_of(p.seq_lens, b, max_len, p.err);
+  for (int b = tid; b < B; b += C::kThreads) prefix[b + 1] = nblk_of(p, b, max_len);
   if (tid == 0) prefix[0] = 0;
   __syncthreads();
   if (warp == 0) {
@@ -204,7 +198,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     const int r = (int)(u - (int64_t)Hg * prefix[lo]);
     cur.hk = r / cur.nblk;  // head box index
     cur.k = r - cur.hk * cur.nblk;
-    cur.L = seq_len_of(p.seq_lens, cur.b, max_len);
+    cur.L = seq_len_of(p, cur.b, max_len);
     cur.u = u;
     return cur;
   };
@@ -218,7 +212,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         do { ++cur.b; } while (cur.b < B && prefix[cur.b + 1] == prefix[cur.b]);
         if (cur.b < B) {
           cur.nblk = prefix[cur.b + 1] - prefix[cur.b];
-          cur.L = seq_len_of(p.seq_lens, cur.b, max_len);
+          cur.L = seq_len_of(p, cur.b, max_len);
         }
       }
     }
@@ -295,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     for (int x = 0; x < kOpsPerLane; ++x) full_geom[x] = geom(NBS, lane + 32 * x);
     // raw block_table entries of this lane's ops in the stage at cu (loads only)
     auto fetch = [&](const Cursor& cu, int nbs, int (&pg)[kOpsPerLane]) {
-      const int32_t* bt = p.block_table + (int64_t)cu.b * p.max_blocks;
+      const int32_t* bt = p.block_table + page_list_start(p.kv_indptr, p.max_blocks, cu.b);
 #pragma unroll
       for (int x = 0; x < kOpsPerLane; ++x) {
         const OpGeom g = nbs == NBS ? full_geom[x] : geom(nbs, lane + 32 * x);
@@ -587,7 +581,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   __shared__ long long red[2][4];
   long long before = 0, total = 0;
   for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
-    const int nb = (seq_len_of(p.seq_lens, i, max_len) + 15) >> 4;
+    const int nb = (seq_len_of(p, i, max_len) + 15) >> 4;
     total += nb;
     if (i < b) before += nb;
   }
@@ -600,7 +594,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   __syncthreads();
   before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
   total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  const int nblk = (seq_len_of(p.seq_lens, b, max_len) + 15) >> 4;
+  const int nblk = (seq_len_of(p, b, max_len) + 15) >> 4;
   griddep_wait();
   if (p.pre_chunks > 0) {
     // cascade: the pair's own-key partials (none if the sequence has no key of

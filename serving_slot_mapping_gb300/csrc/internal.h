@@ -37,8 +37,11 @@ struct DecodeParams {
   PoolGeom pool;
   const void* q;          // [B, Hq, D] bf16
   void* out;              // [B, Hq, D] bf16
-  const int32_t* block_table;
-  const int32_t* seq_lens;
+  const int32_t* block_table;      // dense rows, or kv_indices in the CSR form
+  const int32_t* seq_lens;         // dense form
+  const int32_t* kv_indptr;        // CSR form (nullptr: dense), see page_list_start / seq_keys
+  const int32_t* kv_last_page_len; // CSR form
+  int64_t kv_len;                  // CSR form: entries of kv_indices
   float* part_o;          // [slots, G, D] fp32 unnormalised partial outputs
   float2* part_ml;        // [slots, G] (running max in log2 units, denominator)
   int32_t heads_per_box;  // HB: KV heads loaded per TMA box (power of two <= 8)
@@ -89,8 +92,11 @@ struct PrefillParams {
   const void* q;          // [T, Hq, D] bf16
   void* out;              // [T, Hq, D] bf16
   const int32_t* query_start_loc;
-  const int32_t* block_table;
-  const int32_t* seq_lens;
+  const int32_t* block_table;      // dense rows, or kv_indices in the CSR form
+  const int32_t* seq_lens;         // dense form
+  const int32_t* kv_indptr;        // CSR form (nullptr: dense)
+  const int32_t* kv_last_page_len; // CSR form
+  int64_t kv_len;                  // CSR form: entries of kv_indices
   int64_t total_q;
   int32_t batch;
   int32_t num_q_heads;
@@ -118,8 +124,11 @@ struct AttnF32Params {
   const float* q;         // [rows, Hq, D]
   float* out;
   const int32_t* query_start_loc;  // null for decode (row b = sequence b, n_b = 1)
-  const int32_t* block_table;
-  const int32_t* seq_lens;
+  const int32_t* block_table;      // dense rows, or kv_indices in the CSR form
+  const int32_t* seq_lens;         // dense form
+  const int32_t* kv_indptr;        // CSR form (nullptr: dense)
+  const int32_t* kv_last_page_len; // CSR form
+  int64_t kv_len;                  // CSR form: entries of kv_indices
   int64_t rows;
   int32_t batch;
   int32_t num_q_heads;

@@ -107,11 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = qe - qs;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
   const int max_len = p.max_blocks * ps;
-  int L = pre ? p.prefix_len : __ldg(p.seq_lens + b);
-  if (L < 0 || L > max_len) {
-    if (tid == 0 && hk == 0 && blockIdx.x == 0) record_error(p.err, ERR_SEQ_LEN, L);
-    L = L < 0 ? 0 : max_len;
-  }
+  const int L = pre ? p.prefix_len
+                    : seq_keys(p.seq_lens, p.kv_indptr, p.kv_last_page_len, p.kv_len, b, ps, max_len,
+                               (tid == 0 && hk == 0 && blockIdx.x == 0) ? p.err : nullptr);
   if (n < 0 || qs < 0 || (int64_t)qe > p.total_q) {
     if (tid == 0 && hk == 0 && blockIdx.x == 0) record_error(p.err, ERR_QUERY_LOC, qs);
     return;
@@ -205,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kpo = ps < kBN ? ps : kBN;  // keys per box
     const int ops = kBN / kpo;
     const uint32_t box_bytes = (uint32_t)kpo * D * 2;
-    const int32_t* bt = p.block_table + (int64_t)b * p.max_blocks;
+    const int32_t* bt = p.block_table + (pre ? 0 : page_list_start(p.kv_indptr, p.max_blocks, b));
     int* page_ring = reinterpret_cast<int*>(smem + C::kPageOff);
     auto fetch = [&](int j) {  // raw block_table entry of this lane's box in tile j, -1 if none
       const int key = j * kBN + lane * kpo;

@@ -228,6 +228,21 @@ def cascade_tables(plan: StepPlan, prefix_pages: int, prefix_len: int):
     return pre, int(prefix_len), own_bt, own_lens
 
 
+def csr_tables(plan: StepPlan):
+    """The plan's page table in CSR form: (kv_indptr int32 [B+1], kv_indices
+    int32 [nnz], kv_last_page_len int32 [B]); each sequence lists its
+    ceil(L/ps) pages, the last one holding L - (n-1)*ps tokens."""
+    ps = plan.page_size
+    indptr, indices, last = [0], [], []
+    for b, L in enumerate(plan.seq_lens.tolist()):
+        n = (L + ps - 1) // ps
+        indices.extend(plan.block_table[b, :n].tolist())
+        indptr.append(len(indices))
+        last.append(L - (n - 1) * ps if n else 0)
+    return (np.asarray(indptr, dtype=np.int32), np.asarray(indices or [0], dtype=np.int32),
+            np.asarray(last, dtype=np.int32))
+
+
 def named_plan(name: str) -> StepPlan:
     table = {
         "gqa_decode": lambda: gqa_decode_plan(),
