@@ -573,6 +573,24 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
             torch.cuda.empty_cache()
         except Exception as ex:  # report, do not hide
             res[name] = {"error": repr(ex)[:200]}
+    try:  # the GQA decode batch with its page table in CSR form
+        plan = wl.named_plan("gqa_decode")
+        rig = DecodeRig(plan, dev)
+        rig.append()
+        ip, ix, last = (torch.from_numpy(a).to(dev) for a in wl.csr_tables(plan))
+        msl = int(plan.seq_lens.max())
+
+        def decode_csr():
+            rig.capi.paged_attention_decode_csr(rig.st.key_pool, rig.st.value_pool, rig.st.q, ip, ix, last,
+                                                plan.scale, max_seq_len=msl, out=rig.out, workspace=rig.ws)
+        g = capture(decode_csr, stream)
+        ms = statistics.mean(timed_graph(g, steps, flush, stream))
+        kvb = wl.decode_kv_bytes(plan) + wl.decode_io_bytes(plan)
+        res["gqa_decode_csr"] = {"decode_ms": round(ms, 5), "kv_GBps": round(kvb / (ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4)}
+        del rig, g
+    except Exception as ex:
+        res["gqa_decode_csr"] = {"error": repr(ex)[:200]}
     try:
         plan = wl.named_plan("chunked_prefill")
         rig = PrefillRig(plan, dev)

@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
       next_stage(nx, nbs_n);
       next_stage(nx, nbs_n);  // this producer's next stage: two ahead
       fetch(nx, nbs_n, pg_n);
-      if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
-      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      // this stage's rows first (its page ids were read an iteration ago), so
+      // a slot is refilled the moment it is freed
       const uint32_t sbase = smem_u32(ring + slot * C::kStageBytes);
       int row[kOpsPerLane];
       uint32_t dst[kOpsPerLane];
@@ -347,6 +347,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         }
       }
       const int issued = __reduce_add_sync(0xffffffffu, mine);
+      if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB * slabs_per_op));
       __syncwarp();
 #pragma unroll
