@@ -26,6 +26,8 @@ What it follows:
   page, summary, and the prefix index of the maxtext page, M5 commit),
   defined plainly as attention over the prefix keys followed by the
   sequence's own keys;
+* fp8 (e4m3) pools with one scale per tensor (:mod:`oracle.kv_fp8`): the
+  quantising append and decode over the values the codes stand for;
 * the compressed (CSR) page-table form ``kv_indptr`` / ``kv_indices`` /
   ``kv_last_page_len`` named by NVIDIA/recsys-examples PR #400
   (KVCacheMetadata).
@@ -51,3 +53,4 @@ from .paged_attention import (  # noqa: F401
     paged_attention_decode_csr,
     paged_attention_prefill_csr,
 )
+from . import kv_fp8  # noqa: F401,E402
