@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -62,7 +62,9 @@ typedef enum pa_status {
 
 typedef enum pa_dtype {
   PA_DTYPE_F32 = 0,        /* float32 pool, q and out                           */
-  PA_DTYPE_BF16 = 1        /* bfloat16 pool, q and out; fp32 accumulation       */
+  PA_DTYPE_BF16 = 1,       /* bfloat16 pool, q and out; fp32 accumulation       */
+  PA_DTYPE_FP8_E4M3 = 2    /* e4m3 pool with k_scale / v_scale; bf16 q, out and
+                              appended rows (decode and append only)            */
 } pa_dtype;
 
 /* One layer's KV page pool (mobius PR #395 "ONNX I/O contract":
@@ -76,6 +78,12 @@ typedef struct pa_kv_pool {
   int32_t num_kv_heads;    /* > 0                                                    */
   int32_t head_dim;        /* > 0                                                    */
   int32_t dtype;           /* pa_dtype                                               */
+  /* e4m3 pools only (ignored otherwise): a stored code c stands for
+   * e4m3(c) * scale; finite and > 0.  The pages name an fp8 KV cache (mobius
+   * build features, maxtext pool-sizing table) without a scheme; one scale per
+   * pool and tensor is the plainest one. */
+  float k_scale;
+  float v_scale;
 } pa_kv_pool;
 
 /*
@@ -86,15 +94,19 @@ typedef struct pa_kv_pool {
  *       key_pool.flat[slot_mapping[t]]   = key[t]
  *       value_pool.flat[slot_mapping[t]] = value[t]
  *
- * key, value    device [num_tokens, num_kv_heads, head_dim], pool dtype.
+ * key, value    device [num_tokens, num_kv_heads, head_dim], pool dtype
+ *               (bf16 for an e4m3 pool, 16-byte aligned: each element x is
+ *               stored as e4m3_rn_satfinite(float32(x) / float32(scale)) --
+ *               round to nearest even, magnitudes past 448 saturate, NaN
+ *               stays NaN -- with the pool's k_scale / v_scale).
  * slot_mapping  device int64 [num_tokens]; entry = page_id * page_size +
  *               offset.  A negative entry marks a padding token (skipped).
  *               Entries must be unique within one call (otherwise which
  *               row lands is unspecified).  An entry >= num_pages*page_size
  *               is recorded in the device error word and skipped.
  * num_tokens    >= 0; 0 launches nothing.
- * The write is a bit copy: the pool afterwards is bit-identical to the
- * ScatterND result.
+ * The write is a bit copy (for f32 / bf16 pools): the pool afterwards is
+ * bit-identical to the ScatterND result.
  */
 pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* value,
                           const int64_t* slot_mapping, int64_t num_tokens, void* stream);
@@ -123,6 +135,9 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  *               partial it reads.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
  * query heads per KV head, q 16-byte aligned;
+ * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of
+ * the values the codes stand for (scale * k_scale * q . e4m3(K), outputs
+ * times v_scale), computed with f16 products (every e4m3 value is an f16);
  * f32 path: head_dim <= 256, any page_size.
  */
 size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
@@ -234,7 +249,7 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
  * - All calls share the one array, which keeps the last call's contents;
  *   calls whose kernels overlap on the GPU (different streams, or unordered
  *   host threads) race on it.  No part of it needs to start zeroed.
- * - bf16 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
+ * - bf16 and e4m3 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
  *   workspace anyway).  A call whose partials would not fit, i.e. when
  *   paged_attention_decode_workspace_size(...) exceeds
  *   PA_DECODE_STATIC_SCRATCH_BYTES, returns PA_ERR_WORKSPACE and launches
@@ -268,7 +283,7 @@ pa_status paged_attention_decode_static_scratch(const pa_kv_pool* pool, const vo
  * max_q_len        host upper bound of n_b (sizes the launch).
  * block_table, seq_lens, max_seq_len, scale: as for decode.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most
- * 32 query heads per KV head;
+ * 32 query heads per KV head; e4m3 pools: PA_ERR_UNSUPPORTED;
  * f32 path: head_dim <= 256, any page_size.
  */
 pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out,

@@ -27,6 +27,7 @@ PA_ERR_ALIGN = 8
 
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1
+PA_DTYPE_FP8_E4M3 = 2
 
 # Every symbol include/paged_attn.h declares, with (restype, argtypes).
 _c_void_p = ctypes.c_void_p
@@ -35,7 +36,8 @@ _i32, _i64, _sz, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.
 
 class PaKvPool(ctypes.Structure):
     _fields_ = [("key_pool", _c_void_p), ("value_pool", _c_void_p), ("num_pages", _i64),
-                ("page_size", _i32), ("num_kv_heads", _i32), ("head_dim", _i32), ("dtype", _i32)]
+                ("page_size", _i32), ("num_kv_heads", _i32), ("head_dim", _i32), ("dtype", _i32),
+                ("k_scale", _f32), ("v_scale", _f32)]
 
 
 _PPOOL = ctypes.POINTER(PaKvPool)
@@ -99,6 +101,8 @@ def _dtype_code(t: torch.dtype) -> int:
         return PA_DTYPE_BF16
     if t == torch.float32:
         return PA_DTYPE_F32
+    if t == torch.float8_e4m3fn:
+        return PA_DTYPE_FP8_E4M3
     raise TypeError(f"unsupported pool dtype {t}")
 
 
@@ -123,8 +127,10 @@ def _contig(t: torch.Tensor, name: str):
     return t
 
 
-def make_pool(key_pool: torch.Tensor, value_pool: torch.Tensor) -> PaKvPool:
-    """Describe a [num_pages, page_size, num_kv_heads, head_dim] K/V pool pair."""
+def make_pool(key_pool: torch.Tensor, value_pool: torch.Tensor, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> PaKvPool:
+    """Describe a [num_pages, page_size, num_kv_heads, head_dim] K/V pool pair
+    (float32, bfloat16, or float8_e4m3fn with per-tensor k_scale / v_scale)."""
     if key_pool.shape != value_pool.shape or key_pool.dtype != value_pool.dtype:
         raise ValueError("key_pool and value_pool must match in shape and dtype")
     if key_pool.dim() != 4:
@@ -133,19 +139,23 @@ def make_pool(key_pool: torch.Tensor, value_pool: torch.Tensor) -> PaKvPool:
     _contig(value_pool, "value_pool")
     P, ps, hkv, d = key_pool.shape
     return PaKvPool(key_pool.data_ptr(), value_pool.data_ptr(), P, ps, hkv, d,
-                    _dtype_code(key_pool.dtype))
+                    _dtype_code(key_pool.dtype), float(k_scale), float(v_scale))
 
 
-def paged_kv_append(key_pool, value_pool, key, value, slot_mapping, stream=None):
-    """Scatter ``key/value [T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 [T])."""
-    pool = make_pool(key_pool, value_pool)
+def paged_kv_append(key_pool, value_pool, key, value, slot_mapping, stream=None, k_scale=1.0,
+                    v_scale=1.0):
+    """Scatter ``key/value [T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 [T]).
+
+    e4m3 pools take bf16 rows and store their codes with the given scales."""
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
+    row_dtype = torch.bfloat16 if key_pool.dtype == torch.float8_e4m3fn else key_pool.dtype
     T = slot_mapping.numel()
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
     for n, t in (("key", key), ("value", value)):
         _contig(t, n)
-        if t.dtype != key_pool.dtype or t.numel() != T * pool.num_kv_heads * pool.head_dim:
-            raise ValueError(f"{n} must be [T, num_kv_heads, head_dim] in the pool dtype")
+        if t.dtype != row_dtype or t.numel() != T * pool.num_kv_heads * pool.head_dim:
+            raise ValueError(f"{n} must be [T, num_kv_heads, head_dim] of {row_dtype}")
     st = lib().paged_kv_append(ctypes.byref(pool), _ptr(key), _ptr(value), _ptr(slot_mapping), T,
                                _stream(stream))
     _check(st, "paged_kv_append")
@@ -166,14 +176,15 @@ def decode_workspace(batch, num_q_heads, key_pool, device=None) -> Optional[torc
 
 
 def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale,
-                           max_seq_len=None, out=None, workspace=None, stream=None):
+                           max_seq_len=None, out=None, workspace=None, stream=None, k_scale=1.0,
+                           v_scale=1.0):
     """Decode attention: ``q [B, Hq, D]`` -> ``out [B, Hq, D]``.
 
     ``block_table`` int32 [B, max_blocks]; ``seq_lens`` int32 [B] (after the
     append).  ``max_seq_len`` defaults to max_blocks * page_size (an upper
-    bound needs no device read).
+    bound needs no device read).  ``k_scale`` / ``v_scale`` apply to e4m3 pools.
     """
-    pool = make_pool(key_pool, value_pool)
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
     _contig(q, "q")
     _contig(block_table, "block_table")
     B, hq, d = q.shape
@@ -195,13 +206,14 @@ def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale
 
 
 def paged_attention_decode_static_scratch(key_pool, value_pool, q, block_table, seq_lens, scale,
-                                          max_seq_len=None, out=None, stream=None):
+                                          max_seq_len=None, out=None, stream=None, k_scale=1.0,
+                                          v_scale=1.0):
     """Decode attention whose scratch is the library's own static device array.
 
     For callers that may not allocate device memory; see the header for the
     size limit and the sharing rules of that array.
     """
-    pool = make_pool(key_pool, value_pool)
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
     _contig(q, "q")
     _contig(block_table, "block_table")
     B, hq, d = q.shape
@@ -306,11 +318,12 @@ def _csr_args(kv_indptr, kv_indices, kv_last_page_len):
 
 
 def paged_attention_decode_csr(key_pool, value_pool, q, kv_indptr, kv_indices, kv_last_page_len,
-                               scale, max_seq_len, out=None, workspace=None, stream=None):
+                               scale, max_seq_len, out=None, workspace=None, stream=None, k_scale=1.0,
+                               v_scale=1.0):
     """Decode with the page table in CSR form: sequence b's pages are
     ``kv_indices[kv_indptr[b]:kv_indptr[b+1]]``, its last page holds
     ``kv_last_page_len[b]`` tokens (all int32 device tensors)."""
-    pool = make_pool(key_pool, value_pool)
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
     _contig(q, "q")
     B, hq, d = q.shape
     ip, ix, nix, last = _csr_args(kv_indptr, kv_indices, kv_last_page_len)

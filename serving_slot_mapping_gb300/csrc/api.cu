@@ -57,11 +57,17 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : (dtype == PA_DTYPE_FP8_E4M3 ? 1 : 2); }
+
+bool kv8(const pa_kv_pool* pool) { return pool->dtype == PA_DTYPE_FP8_E4M3; }
 
 pa_status check_pool(const pa_kv_pool* pool) {
   if (pool == nullptr || pool->key_pool == nullptr || pool->value_pool == nullptr) return PA_ERR_NULL;
-  if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16) return PA_ERR_DTYPE;
+  if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16 && pool->dtype != PA_DTYPE_FP8_E4M3)
+    return PA_ERR_DTYPE;
+  if (kv8(pool) && !(std::isfinite(pool->k_scale) && pool->k_scale > 0.f && std::isfinite(pool->v_scale) &&
+                     pool->v_scale > 0.f))
+    return PA_ERR_RANGE;
   if (pool->num_pages <= 0 || pool->page_size <= 0 || pool->num_kv_heads <= 0 || pool->head_dim <= 0)
     return PA_ERR_SHAPE;
   if (pool->num_pages > INT32_MAX) return PA_ERR_RANGE;
@@ -92,7 +98,7 @@ pa_status check_attention(const pa_kv_pool* pool, int32_t batch, int32_t num_q_h
   if ((int64_t)max_blocks_per_seq * pool->page_size > INT32_MAX) return PA_ERR_RANGE;
   if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->page_size) return PA_ERR_SHAPE;
   if (!std::isfinite(scale)) return PA_ERR_RANGE;
-  if (pool->dtype == PA_DTYPE_BF16) {
+  if (pool->dtype != PA_DTYPE_F32) {  // bf16 and e4m3: the TMA / tensor-core paths
     if (pool->head_dim != 64 && pool->head_dim != 128) return PA_ERR_UNSUPPORTED;
     // page-sized TMA boxes of 8-slot blocks
     if (!is_pow2(pool->page_size) || pool->page_size < 8) return PA_ERR_UNSUPPORTED;
@@ -145,7 +151,7 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
   if (key == nullptr || value == nullptr || slot_mapping == nullptr) return PA_ERR_NULL;
   if (!aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
   const size_t es = elem_size(pool->dtype);
-  pa::AppendParams p;
+  pa::AppendParams p{};
   p.key_pool = pool->key_pool;
   p.value_pool = pool->value_pool;
   p.key = key;
@@ -155,6 +161,16 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
   p.num_slots = pool->num_pages * (int64_t)pool->page_size;
   p.row_bytes = (int64_t)pool->num_kv_heads * pool->head_dim * (int64_t)es;
   p.err = error_word();
+  if (kv8(pool)) {  // bf16 rows in, e4m3 codes out, 8 elements per step
+    if (p.row_bytes % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(pool->key_pool, 8) || !aligned(pool->value_pool, 8))
+      return PA_ERR_ALIGN;
+    p.kv8 = 1;
+    p.k_scale = pool->k_scale;
+    p.v_scale = pool->v_scale;
+    cudaError_t e = pa::launch_append(p, 8, num_sms(), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   int vec = 16;
   while (vec > (int)es && ((p.row_bytes % vec) != 0 || !aligned(key, vec) || !aligned(value, vec) ||
                            !aligned(pool->key_pool, vec) || !aligned(pool->value_pool, vec)))
@@ -166,7 +182,7 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
 
 size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                              int32_t head_dim, int32_t dtype) {
-  if (dtype != PA_DTYPE_BF16) return 0;
+  if (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3) return 0;
   if (num_kv_heads <= 0 || num_q_heads <= 0) return 0;
   // heads per box for page_size >= 16 is an upper bound for every page size
   const int hb = pa::decode_heads_per_box(num_kv_heads, num_q_heads / num_kv_heads, 16);
@@ -219,7 +235,8 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PA_ERR_ALIGN;
   const int budget = max_smem_optin();
-  if (pa::decode_smem_bytes(pool->head_dim, group, batch, hb, budget) > (size_t)budget) return PA_ERR_UNSUPPORTED;
+  if (pa::decode_smem_bytes(pool->head_dim, group, batch, hb, budget, kv8(pool)) > (size_t)budget)
+    return PA_ERR_UNSUPPORTED;
   const int64_t slots = pa::decode_partial_slots(batch, pool->num_kv_heads, ctas, hb);
   *p = pa::DecodeParams{};
   p->pool = geom(pool);
@@ -240,7 +257,10 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   p->num_ctas = ctas;
   p->heads_per_box = hb;
   p->smem_budget = budget;
-  p->scale_log2 = (float)((double)scale * kLog2e);
+  // e4m3 pools: S = scale * k_scale * q . e4m3(K), O = v_scale * softmax(S) e4m3(V)
+  p->kv8 = kv8(pool) ? 1 : 0;
+  p->scale_log2 = (float)((double)scale * (kv8(pool) ? (double)pool->k_scale : 1.0) * kLog2e);
+  p->v_scale = kv8(pool) ? pool->v_scale : 1.f;
   p->err = error_word();
   return PA_OK;
 }
@@ -333,6 +353,7 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
                        int32_t max_seq_len, float scale, void* stream) {
   pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
   if (st != PA_OK) return st;
+  if (kv8(pool)) return PA_ERR_UNSUPPORTED;  // e4m3 pools: decode and append only
   if (total_q < 0 || max_q_len < 0 || total_q > INT32_MAX) return PA_ERR_SHAPE;
   if (batch == 0 || total_q == 0) return PA_OK;
   if (max_q_len == 0) return PA_ERR_SHAPE;

@@ -6,7 +6,8 @@
 // elements each, contiguous in both source and pool) are copied with
 // 16-byte vector loads/stores when alignment allows.  The loads bypass L1
 // (read once); the stores keep the default policy so that the attention
-// kernel that runs next finds the fresh rows in L2.
+// kernel that runs next finds the fresh rows in L2.  An e4m3 pool takes bf16
+// rows and stores their codes (quantize8).
 #include "common.cuh"
 #include "internal.h"
 
@@ -52,12 +53,53 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   }
 }
 
+// e4m3 pools: eight bf16 elements (one 16-byte load) become eight codes (one
+// 8-byte store); code = e4m3_rn_satfinite(x / scale) with an IEEE division.
+__device__ __forceinline__ uint2 quantize8(uint4 v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    c[j] = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[j] << 16), scale),
+                           __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), scale));
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+__global__ void __launch_bounds__(256) append_e4m3_kernel(AppendParams p) {
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int64_t n8 = p.row_bytes / 8;  // groups of 8 elements (row_bytes = elements)
+  for (int64_t t = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); t < p.num_tokens;
+       t += (int64_t)gridDim.x * warps) {
+    const int64_t slot = __ldg(p.slot_mapping + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= p.num_slots) {
+      if (lane == 0) record_error(p.err, ERR_SLOT, slot);
+      continue;
+    }
+    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(p.key) + t * p.row_bytes * 2);
+    const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const char*>(p.value) + t * p.row_bytes * 2);
+    uint2* kd = reinterpret_cast<uint2*>(static_cast<char*>(p.key_pool) + slot * p.row_bytes);
+    uint2* vd = reinterpret_cast<uint2*>(static_cast<char*>(p.value_pool) + slot * p.row_bytes);
+    for (int64_t i = lane; i < n8; i += 32) {
+      const uint4 a = __ldcs(ks + i), b = __ldcs(vs + i);
+      kd[i] = quantize8(a, p.k_scale);
+      vd[i] = quantize8(b, p.v_scale);
+    }
+  }
+}
+
 cudaError_t launch_append(const AppendParams& p, int vec_bytes, int num_sms, cudaStream_t s) {
   if (p.num_tokens <= 0) return cudaSuccess;
   const int threads = 256, warps = threads / 32;
   int64_t blocks = (p.num_tokens + warps - 1) / warps;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
+  if (p.kv8) {
+    append_e4m3_kernel<<<(int)blocks, threads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   switch (vec_bytes) {
     case 16: append_kernel<uint4><<<(int)blocks, threads, 0, s>>>(p); break;
     case 8: append_kernel<uint2><<<(int)blocks, threads, 0, s>>>(p); break;

@@ -72,46 +72,55 @@ struct Cursor {
 };
 
 // Compile-time shape of one configuration: HB heads per box, RT row tiles.
-template <int D, int HB, int RT>
+template <int D, int HB, int RT, bool KV8 = false>
 struct Cfg {
   static constexpr int kConsumers = 8;
   static constexpr int NBS = kConsumers / (HB * RT);      // blocks per stage
   static constexpr int kKvProducers = 2;                  // KV producer warps, alternating stages
   static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1);  // + Q producer warp
-  static constexpr int kSlabs = D / 64;                   // 128-byte swizzle slabs per row
-  static constexpr int kHeadTile = 16 * 128;              // one head, 16 rows, one slab
-  static constexpr int kBoxBytes = HB * kHeadTile;        // one {64, 16, HB} box
+  // bf16 pools land as 128-byte-swizzled slabs of 64 dims; e4m3 pools land
+  // unswizzled, a whole row of D codes per slot
+  static constexpr int kSlabs = KV8 ? 1 : D / 64;          // TMA slabs per row
+  static constexpr int kRowBytes = KV8 ? D : 128;         // bytes of one slot row of one slab
+  static constexpr int kHeadTile = 16 * kRowBytes;        // one head, 16 rows, one slab
+  static constexpr int kBoxBytes = HB * kHeadTile;        // one {row, 16, HB} box
   static constexpr int kTensorBytes = NBS * kSlabs * kBoxBytes;
   static constexpr int kStageBytes = 2 * kTensorBytes;    // K then V
+  // e4m3: each consumer warp converts its head's K and V tile to f16 in the
+  // bf16 layout ([64-dim slab][16 rows][128 B], swizzled) before its MMAs
+  static constexpr int kStagingTile = (D / 64) * 16 * 128;             // one tensor, one head
+  static constexpr int kStagingBytes = KV8 ? kConsumers * 2 * kStagingTile : 0;
 };
 
 // Runtime shared-memory layout (stage count depends on G and B).
 struct Layout {
-  int stages, qslot, bar_off, mrg_off, prefix_off, total;
+  int stages, qslot, bar_off, mrg_off, prefix_off, staging_off, total;
 };
 
-template <int D, int HB, int RT>
+template <int D, int HB, int RT, bool KV8 = false>
 __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
-  using C = Cfg<D, HB, RT>;
+  using C = Cfg<D, HB, RT, KV8>;
   Layout L;
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
-  const int fixed = 2 * L.qslot + (2 * 8 + 4) * 8 + merge + (B + 1) * 4 + 1024;
+  const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
+  const int fixed = 2 * L.qslot + (2 * 8 + 4) * 8 + merge + prefix + 128 + C::kStagingBytes + 1024;
   int s = (budget - fixed) / C::kStageBytes;
   if (s > 8) s = 8;
   L.stages = s;
   L.bar_off = s * C::kStageBytes + 2 * L.qslot;
   L.mrg_off = L.bar_off + (2 * s + 4) * 8;
   L.prefix_off = L.mrg_off + merge;
-  L.total = L.prefix_off + (B + 1) * 4 + 1024;
+  L.staging_off = (L.prefix_off + prefix + 127) / 128 * 128;  // 16-byte vector stores
+  L.total = L.staging_off + C::kStagingBytes + 1024;
   return L;
 }
 
-template <int D, int HB, int RT>
-__global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
+template <int D, int HB, int RT, bool KV8>
+__global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         DecodeParams p) {
-  using C = Cfg<D, HB, RT>;
+  using C = Cfg<D, HB, RT, KV8>;
   constexpr int NBS = C::NBS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
   const int Hkv = p.pool.num_kv_heads;
   const int Hg = Hkv / HB;  // head boxes per sequence
   const int Hq = p.num_q_heads;
-  const Layout lay = make_layout<D, HB, RT>(G, B, p.smem_budget);
+  const Layout lay = make_layout<D, HB, RT, KV8>(G, B, p.smem_budget);
   const int S = lay.stages;
   unsigned char* ring = smem;
   unsigned char* qring = smem + S * C::kStageBytes;
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
       g.sl = sub / (16 / R);
       g.jj = (op / boxes_per_block) % nbs;
       g.TT = op / (boxes_per_block * nbs);
-      g.off = (uint32_t)(((g.TT * NBS + g.jj) * C::kSlabs + g.sl) * C::kBoxBytes + g.q * R * 128);
+      g.off = (uint32_t)(((g.TT * NBS + g.jj) * C::kSlabs + g.sl) * C::kBoxBytes + g.q * R * C::kRowBytes);
       return g;
     };
     // every stage but a segment's last has NBS blocks: its geometry is fixed per lane
@@ -349,13 +358,16 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
       const int issued = __reduce_add_sync(0xffffffffu, mine);
       if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * 128 * HB * slabs_per_op));
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * C::kRowBytes * HB * slabs_per_op));
       __syncwarp();
 #pragma unroll
       for (int x = 0; x < kOpsPerLane; ++x) {
         if (row[x] < 0) continue;
         const OpGeom g = nbs == NBS ? full_geom[x] : geom(nbs, lane + 32 * x);
-        tma_load_4d(dst[x], g.TT ? &tmap_v : &tmap_k, 0, row[x], cur.hk * HB, g.sl, full_bar(slot));
+        if (KV8)
+          tma_load_3d(dst[x], g.TT ? &tmap_v : &tmap_k, 0, row[x], cur.hk * HB, full_bar(slot));
+        else
+          tma_load_4d(dst[x], g.TT ? &tmap_v : &tmap_k, 0, row[x], cur.hk * HB, g.sl, full_bar(slot));
       }
       cur = nx;
       nbs = nbs_n;
@@ -396,6 +408,10 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         qf[kk][1] = rB < G ? qsm[(rB * D + d0) >> 1] : 0u;
         qf[kk][2] = rA < G ? qsm[(rA * D + d0 + 8) >> 1] : 0u;
         qf[kk][3] = rB < G ? qsm[(rB * D + d0 + 8) >> 1] : 0u;
+        if (KV8) {  // the MMAs against e4m3 K/V run in f16
+#pragma unroll
+          for (int j = 0; j < 4; ++j) qf[kk][j] = bf16x2_to_f16x2(qf[kk][j]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty_bar(qs));
@@ -414,7 +430,40 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         unsigned char* kt = st + (jw * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
         unsigned char* vt = st + ((NBS + jw) * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
         const int valid = cc.L - (first_k + done + jw) * 16;  // >= 1
-        if (valid < 16) {
+        // tiles the MMAs read, in the 128-byte-swizzled bf16 layout: the stage
+        // itself (bf16 pools) or this warp's f16 copy of it (e4m3 pools)
+        constexpr int kSlabStride = KV8 ? 16 * 128 : C::kBoxBytes;
+        if (KV8) {
+          // e4m3 -> f16 (exact): lane l converts row l / 2, dims (l % 2) * D/2 ..
+          // of K and V; V rows past L_b become 0 (they may hold stale or
+          // poisoned codes and meet P = 0; K rows there are masked below)
+          unsigned char* ks = smem + lay.staging_off + warp * 2 * C::kStagingTile;
+          unsigned char* vs = ks + C::kStagingTile;
+          const int row = lane >> 1, d0 = (lane & 1) * (D / 2);
+          const uint4* ksrc = reinterpret_cast<const uint4*>(kt + row * D + d0);
+          const uint4* vsrc = reinterpret_cast<const uint4*>(vt + row * D + d0);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {  // 16 codes = 2 f16 chunks of 8 per step
+            const uint4 kc = ksrc[c];
+            const uint4 vc = row < valid ? vsrc[c] : make_uint4(0u, 0u, 0u, 0u);
+            const int d = d0 + c * 16;                        // first dim of these 16
+            const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w}, vw[4] = {vc.x, vc.y, vc.z, vc.w};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {                   // 8 dims = one 16-byte chunk
+              const int ch = (d + hh * 8) >> 3;                // chunk index over the row
+              const uint32_t off = (uint32_t)sw128(row, ch, 16 * 128);
+              *reinterpret_cast<uint4*>(ks + off) =
+                  make_uint4(e4m3x2_to_f16x2(kw[2 * hh] & 0xFFFF), e4m3x2_to_f16x2(kw[2 * hh] >> 16),
+                             e4m3x2_to_f16x2(kw[2 * hh + 1] & 0xFFFF), e4m3x2_to_f16x2(kw[2 * hh + 1] >> 16));
+              *reinterpret_cast<uint4*>(vs + off) =
+                  make_uint4(e4m3x2_to_f16x2(vw[2 * hh] & 0xFFFF), e4m3x2_to_f16x2(vw[2 * hh] >> 16),
+                             e4m3x2_to_f16x2(vw[2 * hh + 1] & 0xFFFF), e4m3x2_to_f16x2(vw[2 * hh + 1] >> 16));
+            }
+          }
+          __syncwarp();
+          kt = ks;
+          vt = vs;
+        } else if (valid < 16) {
           // rows past L_b may hold stale or poisoned data: zero them in V (K is masked below)
           for (int e = lane; e < (16 - valid) * C::kSlabs * 8; e += 32) {
             const int row = valid + e / (C::kSlabs * 8);
@@ -431,9 +480,14 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kBoxBytes), b0, b1, b2, b3);
-          mma_bf16_16816(s[0], qf[kk], b0, b1);
-          mma_bf16_16816(s[1], qf[kk], b2, b3);
+          ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), kSlabStride), b0, b1, b2, b3);
+          if (KV8) {
+            mma_f16_16816(s[0], qf[kk], b0, b1);
+            mma_f16_16816(s[1], qf[kk], b2, b3);
+          } else {
+            mma_bf16_16816(s[0], qf[kk], b0, b1);
+            mma_bf16_16816(s[1], qf[kk], b2, b3);
+          }
         }
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -470,18 +524,30 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         m0 = mn0;
         m1 = mn1;
         uint32_t pa[4];
-        pa[0] = pack_bf16(p_[0][0], p_[0][1]);
-        pa[1] = pack_bf16(p_[0][2], p_[0][3]);
-        pa[2] = pack_bf16(p_[1][0], p_[1][1]);
-        pa[3] = pack_bf16(p_[1][2], p_[1][3]);
+        if (KV8) {
+          pa[0] = pack_f16(p_[0][0], p_[0][1]);
+          pa[1] = pack_f16(p_[0][2], p_[0][3]);
+          pa[2] = pack_f16(p_[1][0], p_[1][1]);
+          pa[3] = pack_f16(p_[1][2], p_[1][3]);
+        } else {
+          pa[0] = pack_bf16(p_[0][0], p_[0][1]);
+          pa[1] = pack_bf16(p_[0][2], p_[0][3]);
+          pa[2] = pack_bf16(p_[1][0], p_[1][1]);
+          pa[3] = pack_bf16(p_[1][2], p_[1][3]);
+        }
 #pragma unroll
         for (int jj = 0; jj < D / 16; ++jj) {
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kBoxBytes), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * jj], pa, b0, b1);
-          mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+          ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), kSlabStride), b0, b1, b2, b3);
+          if (KV8) {
+            mma_f16_16816(o[2 * jj], pa, b0, b1);
+            mma_f16_16816(o[2 * jj + 1], pa, b2, b3);
+          } else {
+            mma_bf16_16816(o[2 * jj], pa, b0, b1);
+            mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+          }
         }
-        if (valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
+        if (!KV8 && valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
@@ -501,7 +567,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)hk * G) * D;
     if (NBS == 1) {
       // this warp holds its rows' whole segment state: write directly
-      const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
+      // v_scale: e4m3 V codes stand for code * v_scale (1 for bf16 pools)
+      const float ia = la > 0.f ? p.v_scale / la : 0.f, ib = lb > 0.f ? p.v_scale / lb : 0.f;
 #pragma unroll
       for (int n8 = 0; n8 < D / 8; ++n8) {
         const int col = n8 * 8 + (lane & 3) * 2;
@@ -549,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT>::kThreads, 1)
         const int64_t hkk = (int64_t)cc.hk * HB + hh;
         if (complete) {
           static_cast<__nv_bfloat16*>(p.out)[((int64_t)cc.b * Hq + hkk * G + g) * D + d] =
-              __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+              __float2bfloat16_rn(den > 0.f ? acc * p.v_scale / den : 0.f);
         } else {
           const int64_t ps_ = (seg_id + c) * HB + hh;
           p.part_o[(ps_ * G + g) * D + d] = acc;
@@ -644,7 +711,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const float inv = den > 0.f ? p.v_scale / den : 0.f;
       // weighted rows, 8 partials at a time with all their loads in flight; a
       // partial of weight 0 (empty, or negligible) is not read
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -720,7 +787,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float inv = den > 0.f ? p.v_scale / den : 0.f;
     // weighted sum of the partial rows: lane owns dims 4*lane .. 4*lane+3 (D <= 128)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -748,28 +815,28 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   }
 }
 
-template <int D, int HB, int RT>
+template <int D, int HB, int RT, bool KV8>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-  using C = Cfg<D, HB, RT>;
-  const Layout lay = make_layout<D, HB, RT>(p.group, p.batch, p.smem_budget);
+  using C = Cfg<D, HB, RT, KV8>;
+  const Layout lay = make_layout<D, HB, RT, KV8>(p.group, p.batch, p.smem_budget);
   if (lay.stages < 2) return cudaErrorInvalidConfiguration;
-  auto kern = decode_split_kernel<D, HB, RT>;
+  auto kern = decode_split_kernel<D, HB, RT, KV8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(p.num_ctas), dim3(C::kThreads), (size_t)lay.total, s, tk, tv, p);
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rt,
                            cudaStream_t s) {
   switch (p.heads_per_box * 10 + rt) {
-    case 81: return launch_split<D, 8, 1>(p, tk, tv, s);
-    case 41: return launch_split<D, 4, 1>(p, tk, tv, s);
-    case 21: return launch_split<D, 2, 1>(p, tk, tv, s);
-    case 11: return launch_split<D, 1, 1>(p, tk, tv, s);
-    case 42: return launch_split<D, 4, 2>(p, tk, tv, s);
-    case 22: return launch_split<D, 2, 2>(p, tk, tv, s);
-    case 12: return launch_split<D, 1, 2>(p, tk, tv, s);
+    case 81: return launch_split<D, 8, 1, KV8>(p, tk, tv, s);
+    case 41: return launch_split<D, 4, 1, KV8>(p, tk, tv, s);
+    case 21: return launch_split<D, 2, 1, KV8>(p, tk, tv, s);
+    case 11: return launch_split<D, 1, 1, KV8>(p, tk, tv, s);
+    case 42: return launch_split<D, 4, 2, KV8>(p, tk, tv, s);
+    case 22: return launch_split<D, 2, 2, KV8>(p, tk, tv, s);
+    case 12: return launch_split<D, 1, 2, KV8>(p, tk, tv, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -797,10 +864,11 @@ int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t ma
   return (int)n;
 }
 
-size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget) {
+size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget, bool kv8) {
   const int rt = group <= 16 ? 1 : 2;
   Layout L;
-#define PA_LAYOUT(DD, HH, RR) L = make_layout<DD, HH, RR>(group, batch, budget)
+#define PA_LAYOUT(DD, HH, RR) \
+  L = kv8 ? make_layout<DD, HH, RR, true>(group, batch, budget) : make_layout<DD, HH, RR, false>(group, batch, budget)
   const int key = (head_dim == 128 ? 1000 : 0) + heads_per_box * 10 + rt;
   switch (key) {
     case 1081: PA_LAYOUT(128, 8, 1); break;
@@ -831,11 +899,17 @@ cudaError_t launch_split_only(const DecodeParams& p, cudaStream_t s) {
   const int R = p.pool.page_size < 16 ? p.pool.page_size : 16;
   const int64_t rows = p.pool.num_pages * (int64_t)p.pool.page_size;
   CUtensorMap tk, tv;
+  if (p.kv8) {
+    if (!encode_pool_tmap_u8(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box) ||
+        !encode_pool_tmap_u8(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box))
+      return cudaErrorInvalidValue;
+    return D == 128 ? launch_split_d<128, true>(p, tk, tv, RT, s) : launch_split_d<64, true>(p, tk, tv, RT, s);
+  }
   const int box_slabs = R == 16 ? D / 64 : 1;
   if (!encode_pool_tmap(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs) ||
       !encode_pool_tmap(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, box_slabs))
     return cudaErrorInvalidValue;
-  return D == 128 ? launch_split_d<128>(p, tk, tv, RT, s) : launch_split_d<64>(p, tk, tv, RT, s);
+  return D == 128 ? launch_split_d<128, false>(p, tk, tv, RT, s) : launch_split_d<64, false>(p, tk, tv, RT, s);
 }
 
 }  // namespace

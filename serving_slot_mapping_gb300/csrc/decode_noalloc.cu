@@ -50,7 +50,7 @@ extern "C" pa_status paged_attention_decode_static_scratch(
     const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
     int32_t max_seq_len, float scale, void* stream) {
   if (pool == nullptr) return PA_ERR_NULL;
-  if (pool->dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (pool->dtype != PA_DTYPE_BF16 && pool->dtype != PA_DTYPE_FP8_E4M3) return PA_ERR_UNSUPPORTED;
   const size_t need = paged_attention_decode_workspace_size(batch, num_q_heads, pool->num_kv_heads,
                                                             pool->head_dim, pool->dtype);
   if (need > (size_t)PA_DECODE_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;

@@ -27,8 +27,11 @@ struct AppendParams {
   const int64_t* slot_mapping;
   int64_t num_tokens;
   int64_t num_slots;      // num_pages * page_size
-  int64_t row_bytes;      // num_kv_heads * head_dim * elem_size
+  int64_t row_bytes;      // num_kv_heads * head_dim * elem_size (of the pool)
   unsigned long long* err;
+  // e4m3 pools: key / value rows are bf16 and are quantised on the way in
+  int32_t kv8;
+  float k_scale, v_scale;
 };
 cudaError_t launch_append(const AppendParams& p, int vec_bytes, int num_sms, cudaStream_t s);
 
@@ -56,6 +59,10 @@ struct DecodeParams {
   // cascade decode: the keys of every sequence start with a shared prefix whose
   // partials (one set per key chunk) are merged in by the combine kernel; the
   // split kernel then never finalises a row itself.  pre_chunks == 0: plain decode.
+  // e4m3 pools: K/V codes (k_scale is folded into scale_log2 on the host);
+  // every finished row is multiplied by v_scale (1 for bf16 pools)
+  int32_t kv8;
+  float v_scale;
   const float* pre_o;     // [pre_chunks, B, Hq, D] fp32 unnormalised
   const float2* pre_ml;   // [pre_chunks, B, Hq] (reference max in log2 units, denominator)
   int32_t pre_chunks;
@@ -70,7 +77,7 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_cascade_bf16(const DecodeParams& p, cudaStream_t s, cudaEvent_t prefix_done);
 // Dynamic shared memory the bf16 decode split kernel needs.
 // (size_t)-1 when no stage ring of >= 2 stages fits the budget.
-size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget);
+size_t decode_smem_bytes(int head_dim, int group, int batch, int heads_per_box, int budget, bool kv8);
 
 // TMA descriptor of a bf16 pool viewed as {64, rows, num_kv_heads,
 // head_dim/64} (strides num_kv_heads*head_dim*2, head_dim*2 and 128 bytes),
@@ -85,6 +92,10 @@ bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_
 // slots % 8 == 0.
 bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
                               int box_blocks);
+// An e4m3 pool as a 3-D tensor {head_dim codes, slots, heads} (unswizzled):
+// one box {head_dim, box_rows, box_heads} lands as [head][row][head_dim B].
+bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
+                         int box_rows, int box_heads);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {

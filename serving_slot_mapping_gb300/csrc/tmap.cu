@@ -66,4 +66,18 @@ bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
+                         int box_rows, int box_heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)rows, (cuuint64_t)num_kv_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)num_kv_heads * head_dim, (cuuint64_t)head_dim};
+  cuuint32_t box[3] = {(cuuint32_t)head_dim, (cuuint32_t)box_rows, (cuuint32_t)box_heads};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa

@@ -42,12 +42,12 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version(L):
-    assert L.pa_abi_version() == 1
+    assert L.pa_abi_version() == 2
     assert b"PA_ERR_SHAPE" in L.pa_status_string(2)
 
 
-def _pool(dtype=capi.PA_DTYPE_BF16, hkv=8, d=128, ps=16, P=64, k=0x10000, v=0x20000):
-    return capi.PaKvPool(k, v, P, ps, hkv, d, dtype)
+def _pool(dtype=capi.PA_DTYPE_BF16, hkv=8, d=128, ps=16, P=64, k=0x10000, v=0x20000, ks=1.0, vs=1.0):
+    return capi.PaKvPool(k, v, P, ps, hkv, d, dtype, ks, vs)
 
 
 FAKE = ctypes.c_void_p(0x40000)  # never dereferenced: every call below fails validation
@@ -122,3 +122,16 @@ def test_cascade_validation(L):
     assert call(p, args(wsb=16)) == capi.PA_ERR_WORKSPACE
     assert call(p, args(batch=0)) == capi.PA_OK
     assert L.paged_attention_decode_cascade_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_F32) == 0
+
+
+def test_e4m3_pool_validation(L):
+    f8 = capi.PA_DTYPE_FP8_E4M3
+    assert _decode(L, _pool(dtype=f8, ks=0.0)) == capi.PA_ERR_RANGE              # scale must be > 0
+    assert _decode(L, _pool(dtype=f8, vs=float("inf"))) == capi.PA_ERR_RANGE
+    assert _decode(L, _pool(dtype=f8), ws=None, wsb=0) == capi.PA_ERR_WORKSPACE  # same workspace as bf16
+    assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, f8) == \
+        L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_BF16)
+    p = _pool(dtype=f8)
+    assert L.paged_attention_prefill(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4,
+                                     FAKE, 64, 0.1, None) == capi.PA_ERR_UNSUPPORTED  # decode and append only
+    assert _decode(L, _pool(dtype=3)) == capi.PA_ERR_DTYPE

@@ -1,0 +1,101 @@
+"""GPU parity for e4m3 (fp8) KV pools: the quantising append bit-exact against
+the oracle's quantiser, and decode against the oracle's attention over the
+values the codes stand for.  The cached tokens' codes are written on the host
+by the oracle; dead slots hold the NaN code, so any read of one shows up as a
+non-finite output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import kv_fp8
+from serving_slot_mapping_gb300 import capi
+from serving_slot_mapping_gb300 import workloads as wl
+
+from _parity import assert_close, bits, to_f64
+
+pytestmark = pytest.mark.gpu
+
+KS, VS = 0.02, 0.03
+
+
+def _fp8_step(plan, device, ks=KS, vs=VS):
+    """(device e4m3 pools after the GPU append, host codes after the oracle append, state)."""
+    st = wl.materialize(plan, device)
+    kc0 = kv_fp8.quantize(to_f64(bits(st.key_pool)), ks)        # NaN (dead slots) -> 0x7F
+    vc0 = kv_fp8.quantize(to_f64(bits(st.value_pool)), vs)
+    kp = torch.from_numpy(kc0).to(device).view(torch.float8_e4m3fn)
+    vp = torch.from_numpy(vc0).to(device).view(torch.float8_e4m3fn)
+    if plan.total_new:
+        capi.paged_kv_append(kp, vp, st.key, st.value, st.slot_mapping, k_scale=ks, v_scale=vs)
+        kc, vc = kv_fp8.paged_kv_append_fp8(kc0, vc0, to_f64(bits(st.key)).astype(np.float32),
+                                            to_f64(bits(st.value)).astype(np.float32), plan.slot_mapping, ks, vs)
+    else:
+        kc, vc = kc0, vc0
+    torch.cuda.synchronize()
+    return kp, vp, kc, vc, st
+
+
+def _codes(t):
+    return t.view(torch.uint8).cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["gqa_decode", "long_small"])
+def test_fp8_append_and_decode(cuda_device, name):
+    plan = (wl.gqa_decode_plan() if name == "gqa_decode" else
+            wl.long_context_plan(hkv=8, batch=12, lo=1000, hi=9000, seed=11))
+    kp, vp, kc, vc, st = _fp8_step(plan, cuda_device)
+    assert np.array_equal(_codes(kp), kc) and np.array_equal(_codes(vp), vc)   # append: every byte
+    out = capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                      max_seq_len=int(plan.seq_lens.max()), k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    seqs = list(range(plan.batch)) if plan.batch <= 32 else list(range(0, plan.batch, 4))
+    exp = kv_fp8.paged_attention_decode_fp8(kc, vc, KS, VS, to_f64(bits(st.q)), plan.block_table, plan.seq_lens,
+                                            plan.scale, seqs=seqs)
+    assert_close(out, exp, "bf16", f"fp8 decode {name}", rows=seqs)
+
+
+@pytest.mark.parametrize("hq,hkv,d,ps", [(32, 1, 128, 16), (16, 4, 64, 8), (8, 8, 128, 64), (32, 8, 64, 16)])
+def test_fp8_decode_ragged(cuda_device, hq, hkv, d, ps):
+    lens = np.array([1, 15, 16, 17, 300, 2049, 64])
+    plan = wl.plan_from_lengths(f"fp8_{hq}_{hkv}_{d}_{ps}", "decode", "bf16", hq, hkv, d, ps, lens - 1,
+                                np.ones(len(lens)), seed=hq + d + ps, extra_free_pages=4)
+    kp, vp, kc, vc, st = _fp8_step(plan, cuda_device, ks=0.05, vs=0.01)
+    assert np.array_equal(_codes(kp), kc) and np.array_equal(_codes(vp), vc)
+    out = capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                      max_seq_len=int(lens.max()), k_scale=0.05, v_scale=0.01)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    exp = kv_fp8.paged_attention_decode_fp8(kc, vc, 0.05, 0.01, to_f64(bits(st.q)), plan.block_table,
+                                            plan.seq_lens, plan.scale)
+    assert_close(out, exp, "bf16", f"fp8 decode {hq}/{hkv}/{d} ps{ps}")
+
+
+def test_fp8_decode_csr_and_static_scratch_match(cuda_device):
+    plan = wl.gqa_decode_plan(batch=9, lo=100, hi=2000, seed=21)
+    kp, vp, kc, vc, st = _fp8_step(plan, cuda_device)
+    msl = int(plan.seq_lens.max())
+    a = capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale, max_seq_len=msl,
+                                    k_scale=KS, v_scale=VS)
+    ip, ix, last = (torch.from_numpy(x).to(cuda_device) for x in wl.csr_tables(plan))
+    b = capi.paged_attention_decode_csr(kp, vp, st.q, ip, ix, last, plan.scale, max_seq_len=msl,
+                                        k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_fp8_quantiser_saturates_and_keeps_nan(cuda_device):
+    """Rows past +-448*scale saturate; NaN rows stay NaN codes (the oracle's rule)."""
+    P, ps, hkv, d = 4, 16, 2, 64
+    kp = torch.zeros((P, ps, hkv, d), dtype=torch.float8_e4m3fn, device=cuda_device)
+    vp = torch.zeros_like(kp)
+    vals = torch.tensor([0.0, -0.0, 1e-9, 3.0, -9.0, 1e4, -1e4, float("nan")], dtype=torch.float32)
+    key = vals.repeat(hkv * d // 8 * 3).reshape(3, hkv, d).to(torch.bfloat16).to(cuda_device)
+    slots = torch.tensor([5, 17, 40], dtype=torch.int64, device=cuda_device)
+    capi.paged_kv_append(kp, vp, key, key.clone(), slots, k_scale=0.5, v_scale=2.0)
+    torch.cuda.synchronize()
+    exp = kv_fp8.quantize(to_f64(bits(key)).astype(np.float32), 0.5)
+    got = _codes(kp).reshape(P * ps, hkv, d)[[5, 17, 40]]
+    assert np.array_equal(got, exp)
+    assert (got == 0x7E).any() and (got == 0xFE).any() and (got == 0x7F).any()
