@@ -573,6 +573,43 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
             torch.cuda.empty_cache()
         except Exception as ex:  # report, do not hide
             res[name] = {"error": repr(ex)[:200]}
+    for name in ["gqa_decode", "long_gqa", "long_mqa"]:  # the same batches on e4m3 pools
+        try:
+            plan = wl.named_plan(name)
+            rig = DecodeRig(plan, dev)
+            ks, vs = 0.02, 0.02
+            # pool codes from torch's own e4m3 conversion (inputs only; the timed
+            # step is the library's quantising append + decode)
+            def to_e4m3(pool, sc):
+                out8 = torch.empty(pool.shape, dtype=torch.float8_e4m3fn, device=pool.device)
+                step = max(1, (256 << 20) // max(1, pool[0].numel() * 4))
+                for i in range(0, pool.shape[0], step):
+                    out8[i:i + step] = (pool[i:i + step].float() / sc).to(torch.float8_e4m3fn)
+                return out8
+            kp8 = to_e4m3(rig.st.key_pool, ks)
+            vp8 = to_e4m3(rig.st.value_pool, vs)
+            del rig.st.key_pool, rig.st.value_pool
+            torch.cuda.empty_cache()
+            msl = int(plan.seq_lens.max())
+            st = rig.st
+
+            def decode_fp8():
+                rig.capi.paged_attention_decode(kp8, vp8, st.q, st.block_table, st.seq_lens, plan.scale,
+                                                max_seq_len=msl, out=rig.out, workspace=rig.ws, k_scale=ks,
+                                                v_scale=vs)
+            g = capture(decode_fp8, stream)
+            ms = statistics.mean(timed_graph(g, steps, flush, stream))
+            kvb = wl.decode_kv_bytes(plan) // 2 + wl.decode_io_bytes(plan)
+            res[name + "_fp8"] = {"decode_ms": round(ms, 5), "kv_GBps": round(kvb / (ms * 1e-3) / 1e9, 1),
+                                  "frac_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
+                                  "tokens_per_s": round(plan.batch / (ms * 1e-3), 1),
+                                  "speedup_vs_bf16_pool": None}
+            if name in res and "decode_ms" in res[name]:
+                res[name + "_fp8"]["speedup_vs_bf16_pool"] = round(res[name]["decode_ms"] / ms, 3)
+            del rig, g, kp8, vp8
+            torch.cuda.empty_cache()
+        except Exception as ex:
+            res[name + "_fp8"] = {"error": repr(ex)[:200]}
     try:  # the GQA decode batch with its page table in CSR form
         plan = wl.named_plan("gqa_decode")
         rig = DecodeRig(plan, dev)

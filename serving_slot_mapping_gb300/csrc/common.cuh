@@ -97,10 +97,17 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Two e4m3 codes (low byte first) as an f16 pair: exact, every e4m3 value is an f16.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes16), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Two e4m3 codes as an f16 pair (first code in the low half), exact: every
+// e4m3 value, NaN included, is an f16.  _lo takes bytes 0-1 of w, _hi 2-3.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}\n" : "=r"(d) : "r"(w));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+  uint32_t d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.rn.f16x2.e4m3x2 %0, hi;\n}\n" : "=r"(d) : "r"(w));
+  return d;
 }
 
 // Two floats (first in the low byte) as e4m3 codes: round to nearest even,

@@ -78,23 +78,32 @@ struct Cfg {
   static constexpr int NBS = kConsumers / (HB * RT);      // blocks per stage
   static constexpr int kKvProducers = 2;                  // KV producer warps, alternating stages
   static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1);  // + Q producer warp
-  // bf16 pools land as 128-byte-swizzled slabs of 64 dims; e4m3 pools land
-  // unswizzled, a whole row of D codes per slot
+  // bf16 pools land as 128-byte-swizzled slabs of 64 dims; e4m3 pools land a
+  // whole row of D codes per slot, swizzled over its D bytes (see sw_e4m3)
   static constexpr int kSlabs = KV8 ? 1 : D / 64;          // TMA slabs per row
   static constexpr int kRowBytes = KV8 ? D : 128;         // bytes of one slot row of one slab
   static constexpr int kHeadTile = 16 * kRowBytes;        // one head, 16 rows, one slab
   static constexpr int kBoxBytes = HB * kHeadTile;        // one {row, 16, HB} box
   static constexpr int kTensorBytes = NBS * kSlabs * kBoxBytes;
   static constexpr int kStageBytes = 2 * kTensorBytes;    // K then V
-  // e4m3: each consumer warp converts its head's K and V tile to f16 in the
-  // bf16 layout ([64-dim slab][16 rows][128 B], swizzled) before its MMAs
-  static constexpr int kStagingTile = (D / 64) * 16 * 128;             // one tensor, one head
-  static constexpr int kStagingBytes = KV8 ? kConsumers * 2 * kStagingTile : 0;
 };
+
+// Most ring stages a CTA keeps (small e4m3 / MQA stages reach it).
+constexpr int kMaxStages = 12;
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in one head's e4m3 tile
+// ([16 rows][D B]) as TMA lands it: the 128-byte swizzle (D = 128: chunk XOR
+// row % 8) or the 64-byte one (D = 64: chunk XOR (row / 2) % 4).  Eight rows
+// of one chunk then sit in eight distinct bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t sw_e4m3(int row, int chunk) {
+  if (D == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
+  return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
 
 // Runtime shared-memory layout (stage count depends on G and B).
 struct Layout {
-  int stages, qslot, bar_off, mrg_off, prefix_off, staging_off, total;
+  int stages, qslot, bar_off, mrg_off, prefix_off, total;
 };
 
 template <int D, int HB, int RT, bool KV8 = false>
@@ -104,15 +113,14 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
-  const int fixed = 2 * L.qslot + (2 * 8 + 4) * 8 + merge + prefix + 128 + C::kStagingBytes + 1024;
+  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
-  if (s > 8) s = 8;
+  if (s > kMaxStages) s = kMaxStages;
   L.stages = s;
   L.bar_off = s * C::kStageBytes + 2 * L.qslot;
   L.mrg_off = L.bar_off + (2 * s + 4) * 8;
   L.prefix_off = L.mrg_off + merge;
-  L.staging_off = (L.prefix_off + prefix + 127) / 128 * 128;  // 16-byte vector stores
-  L.total = L.staging_off + C::kStagingBytes + 1024;
+  L.total = L.prefix_off + prefix + 1024;
   return L;
 }
 
@@ -315,10 +323,12 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     Cursor cur = locate(u0);
     bool alive = true;
     int nbs = stage_blocks(cur);
-    int64_t i = 0;
+    // this producer's next stage index i, kept as ring slot + wrap count
+    // (no division in the loop): slot = i % S, lap = i / S
+    int slot = 0, lap = 0;
     if (pw == 1) {
       next_stage(cur, nbs);
-      i = 1;
+      slot = 1;  // S >= 2
     }
     // page ids of the current and the next stage; the loop is unrolled by two
     // with the buffers swapped, so no register holding a load in flight is
@@ -327,7 +337,6 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     fetch(cur, nbs, pga);  // block_table is an input, not written by the append kernel
     griddep_wait();        // the pool rows of this step were written by the append kernel
     auto stage = [&](int (&pg)[kOpsPerLane], int (&pg_n)[kOpsPerLane]) {
-      const int slot = (int)(i % S);
       Cursor nx = cur;
       int nbs_n = nbs;
       next_stage(nx, nbs_n);
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         }
       }
       const int issued = __reduce_add_sync(0xffffffffu, mine);
-      if (lane == 0 && i >= S && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)(((i / S) - 1) & 1), p.err);
+      if (lane == 0 && lap > 0 && alive) alive = mbar_wait(empty_bar(slot), (uint32_t)((lap - 1) & 1), p.err);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       if (lane == 0) mbar_arrive_expect_tx(full_bar(slot), (uint32_t)(issued * R * C::kRowBytes * HB * slabs_per_op));
       __syncwarp();
@@ -371,7 +380,11 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       }
       cur = nx;
       nbs = nbs_n;
-      i += C::kKvProducers;
+      slot += C::kKvProducers;  // kKvProducers <= S
+      if (slot >= S) {
+        slot -= S;
+        ++lap;
+      }
     };
     while (nbs > 0) {
       stage(pga, pgb);
@@ -389,7 +402,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
   Cursor cc = locate(u0);
-  int64_t i = 0;  // stage index
+  int slot = 0;        // ring slot of the next stage (stage index % S)
+  uint32_t phase = 0;  // its full-barrier parity ((stage index / S) & 1)
   bool alive = true;
   for (int seg = 0; cc.u < u1; ++seg) {
     const int seg_blocks = (int)min((int64_t)(cc.nblk - cc.k), u1 - cc.u);
@@ -403,14 +417,21 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       const uint32_t* qsm = reinterpret_cast<const uint32_t*>(qring + qs * lay.qslot) + (h * G * D) / 2;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int d0 = kk * 16 + (lane & 3) * 2;
-        qf[kk][0] = rA < G ? qsm[(rA * D + d0) >> 1] : 0u;
-        qf[kk][1] = rB < G ? qsm[(rB * D + d0) >> 1] : 0u;
-        qf[kk][2] = rA < G ? qsm[(rA * D + d0 + 8) >> 1] : 0u;
-        qf[kk][3] = rB < G ? qsm[(rB * D + d0 + 8) >> 1] : 0u;
-        if (KV8) {  // the MMAs against e4m3 K/V run in f16
-#pragma unroll
-          for (int j = 0; j < 4; ++j) qf[kk][j] = bf16x2_to_f16x2(qf[kk][j]);
+        if (KV8) {
+          // f16, dims permuted to match the e4m3 K fragments: within a 16-dim
+          // step, MMA k = 2c, 2c + 1 are dims 4c, 4c + 1 and k = 2c + 8, 2c + 9
+          // are dims 4c + 2, 4c + 3 (c = lane % 4)
+          const int d0 = kk * 16 + (lane & 3) * 4;
+          qf[kk][0] = rA < G ? bf16x2_to_f16x2(qsm[(rA * D + d0) >> 1]) : 0u;
+          qf[kk][1] = rB < G ? bf16x2_to_f16x2(qsm[(rB * D + d0) >> 1]) : 0u;
+          qf[kk][2] = rA < G ? bf16x2_to_f16x2(qsm[(rA * D + d0 + 2) >> 1]) : 0u;
+          qf[kk][3] = rB < G ? bf16x2_to_f16x2(qsm[(rB * D + d0 + 2) >> 1]) : 0u;
+        } else {
+          const int d0 = kk * 16 + (lane & 3) * 2;
+          qf[kk][0] = rA < G ? qsm[(rA * D + d0) >> 1] : 0u;
+          qf[kk][1] = rB < G ? qsm[(rB * D + d0) >> 1] : 0u;
+          qf[kk][2] = rA < G ? qsm[(rA * D + d0 + 8) >> 1] : 0u;
+          qf[kk][3] = rB < G ? qsm[(rB * D + d0 + 8) >> 1] : 0u;
         }
       }
       __syncwarp();
@@ -421,54 +442,23 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     for (int n8 = 0; n8 < D / 8; ++n8) o[n8][0] = o[n8][1] = o[n8][2] = o[n8][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int done = 0; done < seg_blocks; ++i) {
+    for (int done = 0; done < seg_blocks;) {
       const int nbs = min(NBS, seg_blocks - done);
-      const int slot = (int)(i % S);
-      if (alive) alive = mbar_wait(full_bar(slot), (uint32_t)((i / S) & 1), p.err);
+      if (alive) alive = mbar_wait(full_bar(slot), phase, p.err);
       if (jw < nbs) {
         unsigned char* st = ring + slot * C::kStageBytes;
         unsigned char* kt = st + (jw * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
         unsigned char* vt = st + ((NBS + jw) * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
         const int valid = cc.L - (first_k + done + jw) * 16;  // >= 1
-        // tiles the MMAs read, in the 128-byte-swizzled bf16 layout: the stage
-        // itself (bf16 pools) or this warp's f16 copy of it (e4m3 pools)
-        constexpr int kSlabStride = KV8 ? 16 * 128 : C::kBoxBytes;
-        if (KV8) {
-          // e4m3 -> f16 (exact): lane l converts row l / 2, dims (l % 2) * D/2 ..
-          // of K and V; V rows past L_b become 0 (they may hold stale or
-          // poisoned codes and meet P = 0; K rows there are masked below)
-          unsigned char* ks = smem + lay.staging_off + warp * 2 * C::kStagingTile;
-          unsigned char* vs = ks + C::kStagingTile;
-          const int row = lane >> 1, d0 = (lane & 1) * (D / 2);
-          const uint4* ksrc = reinterpret_cast<const uint4*>(kt + row * D + d0);
-          const uint4* vsrc = reinterpret_cast<const uint4*>(vt + row * D + d0);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {  // 16 codes = 2 f16 chunks of 8 per step
-            const uint4 kc = ksrc[c];
-            const uint4 vc = row < valid ? vsrc[c] : make_uint4(0u, 0u, 0u, 0u);
-            const int d = d0 + c * 16;                        // first dim of these 16
-            const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w}, vw[4] = {vc.x, vc.y, vc.z, vc.w};
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {                   // 8 dims = one 16-byte chunk
-              const int ch = (d + hh * 8) >> 3;                // chunk index over the row
-              const uint32_t off = (uint32_t)sw128(row, ch, 16 * 128);
-              *reinterpret_cast<uint4*>(ks + off) =
-                  make_uint4(e4m3x2_to_f16x2(kw[2 * hh] & 0xFFFF), e4m3x2_to_f16x2(kw[2 * hh] >> 16),
-                             e4m3x2_to_f16x2(kw[2 * hh + 1] & 0xFFFF), e4m3x2_to_f16x2(kw[2 * hh + 1] >> 16));
-              *reinterpret_cast<uint4*>(vs + off) =
-                  make_uint4(e4m3x2_to_f16x2(vw[2 * hh] & 0xFFFF), e4m3x2_to_f16x2(vw[2 * hh] >> 16),
-                             e4m3x2_to_f16x2(vw[2 * hh + 1] & 0xFFFF), e4m3x2_to_f16x2(vw[2 * hh + 1] >> 16));
-            }
-          }
-          __syncwarp();
-          kt = ks;
-          vt = vs;
-        } else if (valid < 16) {
-          // rows past L_b may hold stale or poisoned data: zero them in V (K is masked below)
-          for (int e = lane; e < (16 - valid) * C::kSlabs * 8; e += 32) {
-            const int row = valid + e / (C::kSlabs * 8);
-            const int rem = e % (C::kSlabs * 8);
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * C::kBoxBytes + row * 128 + (rem & 7) * 16) =
+        if (valid < 16) {
+          // rows past L_b may hold stale or poisoned data (NaN would survive
+          // P = 0): zero them in V; K is masked below.  A row's chunks stay in
+          // the row under either swizzle.
+          constexpr int kCh = C::kRowBytes / 16;  // 16-byte chunks of a row of one slab
+          for (int e = lane; e < (16 - valid) * C::kSlabs * kCh; e += 32) {
+            const int row = valid + e / (C::kSlabs * kCh);
+            const int rem = e % (C::kSlabs * kCh);
+            *reinterpret_cast<uint4*>(vt + (rem / kCh) * C::kBoxBytes + row * C::kRowBytes + (rem % kCh) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
@@ -477,14 +467,24 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         float s[2][4];
 #pragma unroll
         for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+        if (KV8) {
+          // e4m3 K as 16-bit pairs: matrix m = keys (m & 1) * 8 .. + 7 of
+          // 16-dim chunk 2 * q2 + (m >> 1); lane gets 4 codes of key lane / 4,
+          // dims 4c .. 4c + 3: the first two are B register 0, the last two 1
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), kSlabStride), b0, b1, b2, b3);
-          if (KV8) {
-            mma_f16_16816(s[0], qf[kk], b0, b1);
-            mma_f16_16816(s[1], qf[kk], b2, b3);
-          } else {
+          for (int q2 = 0; q2 < D / 32; ++q2) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(kbase + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
+            mma_f16_16816(s[0], qf[2 * q2], e4m3x2_lo_to_f16x2(r0), e4m3x2_hi_to_f16x2(r0));
+            mma_f16_16816(s[1], qf[2 * q2], e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r1));
+            mma_f16_16816(s[0], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r2), e4m3x2_hi_to_f16x2(r2));
+            mma_f16_16816(s[1], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r3));
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kBoxBytes), b0, b1, b2, b3);
             mma_bf16_16816(s[0], qf[kk], b0, b1);
             mma_bf16_16816(s[1], qf[kk], b2, b3);
           }
@@ -535,26 +535,58 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
           pa[2] = pack_bf16(p_[1][0], p_[1][1]);
           pa[3] = pack_bf16(p_[1][2], p_[1][3]);
         }
+        if (KV8) {
+          // e4m3 V, transposed as 16-bit pairs: lane gets keys 2c, 2c + 1 of
+          // dims 2j, 2j + 1 (j = lane / 4) of a 16-dim chunk, regrouped to key
+          // pairs per dim; the even dims form output tile 2 * chunk, the odd
+          // ones tile 2 * chunk + 1, so o[t] column n is dim (t / 2) * 16 + 2n + t % 2
 #pragma unroll
-        for (int jj = 0; jj < D / 16; ++jj) {
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), kSlabStride), b0, b1, b2, b3);
-          if (KV8) {
-            mma_f16_16816(o[2 * jj], pa, b0, b1);
-            mma_f16_16816(o[2 * jj + 1], pa, b2, b3);
-          } else {
+          for (int q2 = 0; q2 < D / 32; ++q2) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4_trans(vbase + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
+            r0 = __byte_perm(r0, 0u, 0x3120);  // (key 2c, key 2c+1) of dim 2j | same of dim 2j+1
+            r1 = __byte_perm(r1, 0u, 0x3120);
+            r2 = __byte_perm(r2, 0u, 0x3120);
+            r3 = __byte_perm(r3, 0u, 0x3120);
+            mma_f16_16816(o[4 * q2], pa, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1));
+            mma_f16_16816(o[4 * q2 + 1], pa, e4m3x2_hi_to_f16x2(r0), e4m3x2_hi_to_f16x2(r1));
+            mma_f16_16816(o[4 * q2 + 2], pa, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3));
+            mma_f16_16816(o[4 * q2 + 3], pa, e4m3x2_hi_to_f16x2(r2), e4m3x2_hi_to_f16x2(r3));
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < D / 16; ++jj) {
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kBoxBytes), b0, b1, b2, b3);
             mma_bf16_16816(o[2 * jj], pa, b0, b1);
             mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
           }
         }
-        if (!KV8 && valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
+        if (valid < 16) fence_proxy_async_smem();  // our zero stores precede the next TMA into this slot
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
       done += nbs;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
 
     // ---- segment end: normalise / merge / write ----
+    // Output pair x (0 .. D/8 - 1) of this lane, for rows rA (half 0) / rB
+    // (half 1): two adjacent dims starting at out_col(x).  bf16 tiles hold
+    // dims t * 8 + 2c, 2c + 1; the e4m3 path's tiles 2k, 2k + 1 hold the even
+    // and odd dims of chunk k, so a lane's adjacent pairs mix the two.
+    auto out_col = [&](int x) {
+      const int k = x >> 1, pi = x & 1, c = lane & 3;
+      return KV8 ? k * 16 + 4 * c + 2 * pi : k * 16 + 8 * pi + 2 * c;
+    };
+    auto out_pair = [&](const float (&acc)[D / 8][4], int x, int half) {
+      const int k = x >> 1, pi = x & 1;
+      return KV8 ? make_float2(acc[2 * k][2 * half + pi], acc[2 * k + 1][2 * half + pi])
+                 : make_float2(acc[2 * k + pi][2 * half], acc[2 * k + pi][2 * half + 1]);
+    };
     float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
     la += __shfl_xor_sync(0xffffffffu, la, 2);
     float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -570,14 +602,15 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       // v_scale: e4m3 V codes stand for code * v_scale (1 for bf16 pools)
       const float ia = la > 0.f ? p.v_scale / la : 0.f, ib = lb > 0.f ? p.v_scale / lb : 0.f;
 #pragma unroll
-      for (int n8 = 0; n8 < D / 8; ++n8) {
-        const int col = n8 * 8 + (lane & 3) * 2;
+      for (int x = 0; x < D / 8; ++x) {
+        const int col = out_col(x);
+        const float2 va = out_pair(o, x, 0), vb = out_pair(o, x, 1);
         if (complete) {
-          if (rA < G) *reinterpret_cast<uint32_t*>(outp + rA * D + col) = pack_bf16(o[n8][0] * ia, o[n8][1] * ia);
-          if (rB < G) *reinterpret_cast<uint32_t*>(outp + rB * D + col) = pack_bf16(o[n8][2] * ib, o[n8][3] * ib);
+          if (rA < G) *reinterpret_cast<uint32_t*>(outp + rA * D + col) = pack_bf16(va.x * ia, va.y * ia);
+          if (rB < G) *reinterpret_cast<uint32_t*>(outp + rB * D + col) = pack_bf16(vb.x * ib, vb.y * ib);
         } else {
-          if (rA < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rA) * D + col) = make_float2(o[n8][0], o[n8][1]);
-          if (rB < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rB) * D + col) = make_float2(o[n8][2], o[n8][3]);
+          if (rA < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rA) * D + col) = va;
+          if (rB < G) *reinterpret_cast<float2*>(p.part_o + (pslot * G + rB) * D + col) = vb;
         }
       }
       if (!complete && (lane & 3) == 0) {
@@ -593,10 +626,10 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         if (rB < G) { mml[rB * 2] = m1; mml[rB * 2 + 1] = lb; }
       }
 #pragma unroll
-      for (int n8 = 0; n8 < D / 8; ++n8) {
-        const int col = n8 * 8 + (lane & 3) * 2;
-        if (rA < G) *reinterpret_cast<float2*>(&mo[rA * D + col]) = make_float2(o[n8][0], o[n8][1]);
-        if (rB < G) *reinterpret_cast<float2*>(&mo[rB * D + col]) = make_float2(o[n8][2], o[n8][3]);
+      for (int x = 0; x < D / 8; ++x) {
+        const int col = out_col(x);
+        if (rA < G) *reinterpret_cast<float2*>(&mo[rA * D + col]) = out_pair(o, x, 0);
+        if (rB < G) *reinterpret_cast<float2*>(&mo[rB * D + col]) = out_pair(o, x, 1);
       }
       named_barrier(1, C::kConsumers * 32);
       for (int idx = tid; idx < HB * G * D; idx += C::kConsumers * 32) {

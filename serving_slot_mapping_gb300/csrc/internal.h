@@ -92,8 +92,9 @@ bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_
 // slots % 8 == 0.
 bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
                               int box_blocks);
-// An e4m3 pool as a 3-D tensor {head_dim codes, slots, heads} (unswizzled):
-// one box {head_dim, box_rows, box_heads} lands as [head][row][head_dim B].
+// An e4m3 pool as a 3-D tensor {head_dim codes, slots, heads}: one box
+// {head_dim, box_rows, box_heads} lands as [head][row][head_dim B], each row's
+// 16-byte chunks swizzled (128-byte swizzle for head_dim 128, 64-byte for 64).
 bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
                          int box_rows, int box_heads);
 

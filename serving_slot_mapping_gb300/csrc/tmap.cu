@@ -74,8 +74,12 @@ bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int n
   cuuint64_t strides[2] = {(cuuint64_t)num_kv_heads * head_dim, (cuuint64_t)head_dim};
   cuuint32_t box[3] = {(cuuint32_t)head_dim, (cuuint32_t)box_rows, (cuuint32_t)box_heads};
   cuuint32_t estr[3] = {1, 1, 1};
+  // a row of head_dim codes is one swizzle span: 128-byte rows (head_dim 128)
+  // take the 128-byte swizzle, 64-byte rows the 64-byte one
+  if (head_dim != 64 && head_dim != 128) return false;
+  const CUtensorMapSwizzle sw = head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
