@@ -132,7 +132,11 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  *               when that size is 0), 16-byte aligned, owned by the caller and
  *               not shared by calls in flight at the same time.  Its
  *               contents need no initialisation: each call writes every
- *               partial it reads.
+ *               partial it reads, and the per-segment arrival counters that
+ *               pick the CTA merging a segment cut across CTAs carry the
+ *               launch's grid id, so a word left by any earlier launch (or
+ *               never written) counts as zero.  The merge runs inside the
+ *               one decode kernel (no second launch).
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
  * query heads per KV head, q 16-byte aligned;
  * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of

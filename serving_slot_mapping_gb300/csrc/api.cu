@@ -118,7 +118,9 @@ size_t decode_ws_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int ct
   if (batch <= 0 || hq <= 0 || hkv <= 0 || d <= 0) return 0;
   const int64_t slots = pa::decode_partial_slots(batch, hkv, ctas, hb);
   const int64_t g = hq / hkv;
-  return align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256);
+  // [launch epoch, grid counter | pad] [partial o] [partial (m, l)] [segment counters]
+  return 256 + align_up((size_t)(slots * g * d * 4), 256) + align_up((size_t)(slots * g * 8), 256) +
+         align_up((size_t)batch * hkv * 8, 256);
 }
 
 }  // namespace
@@ -247,9 +249,12 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   p->kv_indptr = t.indptr;
   p->kv_last_page_len = t.last;
   p->kv_len = t.kv_len;
-  p->part_o = static_cast<float*>(workspace);
+  char* ws = static_cast<char*>(workspace);
+  p->launch_epoch = reinterpret_cast<unsigned long long*>(ws);
+  p->part_o = reinterpret_cast<float*>(ws + 256);
   const size_t o_bytes = align_up((size_t)(slots * group * pool->head_dim * 4), 256);
-  p->part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
+  p->part_ml = reinterpret_cast<float2*>(ws + 256 + o_bytes);
+  p->seg_count = reinterpret_cast<unsigned long long*>(ws + 256 + o_bytes + align_up((size_t)(slots * group * 8), 256));
   p->batch = batch;
   p->num_q_heads = num_q_heads;
   p->group = group;

@@ -71,6 +71,163 @@ struct Cursor {
   int64_t u;
 };
 
+// Count one more arrival on a counter word holding (tag << 16) | arrivals in
+// this launch; a word with another tag (an earlier launch's, or uninitialised
+// memory) counts as 0.  Returns the arrivals before this one.  Once the word
+// carries this launch's tag an arrival is one atomicAdd; only a stale word
+// takes a compare-and-swap, which exactly one arrival wins (a loser re-reads
+// and adds), so each arrival makes at most three atomic operations.  The
+// bound only guards against a broken counter (then a bounded-wait error is
+// recorded and the caller acts as a non-last arrival).
+__device__ __forceinline__ unsigned arrive_part(unsigned long long* cnt, unsigned long long tag,
+                                                unsigned long long* err) {
+  unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(cnt);
+  for (int it = 0; it < 8; ++it) {
+    if ((w >> 16) == tag) {
+      if ((w & 0xFFFFu) == 0xFFFFu) break;  // a full count field: not a live counter
+      const unsigned long long old = atomicAdd(cnt, 1ull);
+      if ((old >> 16) == tag && (old & 0xFFFFu) != 0xFFFFu) return (unsigned)(old & 0xFFFFu);
+      break;
+    }
+    const unsigned long long got = atomicCAS(cnt, w, (tag << 16) | 1ull);
+    if (got == w) return 0u;
+    w = got;
+  }
+  record_error(err, ERR_TIMEOUT, -1);
+  return 0xFFFFFFFFu;
+}
+
+// One warp merges query row (head h of the box, row g) of segment `seg`, cut
+// into parts by CTAs c0 .. c0 + nparts - 1 (a CTA that owns no unit, only
+// possible when U < n, wrote nothing and weighs 0), and writes the bf16
+// result to outrow: o = v_scale * sum_q 2^(m_q - M) o_q / sum_q 2^(m_q - M) l_q.
+// Lane q holds part q's (m, l); each lane accumulates 4 dims.  The first 8
+// parts' rows are loaded together with the (m, l) (one round trip), later
+// parts one by one.
+__device__ __noinline__ void merge_segment_row(const DecodeParams& p, int64_t seg, int HB, int G, int h, int g,
+                                               int c0, int nparts, int64_t U, int n, int D,
+                                               __nv_bfloat16* outrow) {
+  const int lane = threadIdx.x & 31;
+  const bool some_empty = U < n;
+  const bool dims = 4 * lane < D;
+  auto absent = [&](int q) { return some_empty && cta_range_empty(c0 + q, U, n); };
+  auto row = [&](int q) {
+    return __ldcg(reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D) + lane);
+  };
+  auto ml_of = [&](int q) {
+    return absent(q) ? make_float2(-INFINITY, 0.f) : __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
+  };
+  constexpr int kRegParts = 8;
+  float4 vr[kRegParts];
+#pragma unroll
+  for (int q = 0; q < kRegParts; ++q)
+    vr[q] = (q < nparts && dims && !absent(q)) ? row(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float2 ml_mine = lane < nparts ? ml_of(lane) : make_float2(-INFINITY, 0.f);
+  float M = ml_mine.x;
+  for (int q = lane + 32; q < nparts; q += 32) M = fmaxf(M, ml_of(q).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float f_mine = (ml_mine.x == -INFINITY) ? 0.f : fast_exp2(ml_mine.x - M);
+  float den = f_mine * ml_mine.y;
+  for (int q = lane + 32; q < nparts; q += 32) {
+    const float2 ml = ml_of(q);
+    den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = den > 0.f ? p.v_scale / den : 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < kRegParts; ++q) {
+    const float f = __shfl_sync(0xffffffffu, f_mine, q);
+    acc.x += f * vr[q].x; acc.y += f * vr[q].y; acc.z += f * vr[q].z; acc.w += f * vr[q].w;
+  }
+  for (int q = kRegParts; q < nparts; ++q) {
+    float f = __shfl_sync(0xffffffffu, f_mine, q & 31);
+    if (q >= 32) {
+      const float2 ml = ml_of(q);
+      f = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+    }
+    if (f != 0.f && dims) {
+      const float4 v = row(q);
+      acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+    }
+  }
+  if (dims) {
+    uint2 packed;
+    packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(outrow + 4 * lane) = packed;
+  }
+}
+
+// The consumer threads (nthreads, ids tid) merge every query row of segment
+// (b, head box hkb), cut into parts by CTAs c0 .. c0 + span - 1, into the bf16
+// output.  A part's partials are contiguous ([HB*G rows][D] fp32 and
+// [HB*G] (m, l)), so each part is copied whole into shared memory (the idle
+// stage ring, `scratch`) with 16-byte cp.async -- one round trip for all
+// parts -- and every thread then merges 4 dims of a row:
+//   o = v_scale * sum_q 2^(m_q - M) o_q / sum_q 2^(m_q - M) l_q.
+// Parts that do not fit in the ring are merged warp by warp from global memory.
+template <int D>
+__device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb, int c0, int span, int HB, int Hg,
+                                           int64_t U, int n, unsigned char* scratch, int scratch_bytes, int tid,
+                                           int nthreads) {
+  const int G = p.group;
+  const int rows = HB * G;
+  const int64_t seg = (int64_t)b * Hg + hkb;
+  const int64_t Hq = p.num_q_heads;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hkb * HB * G) * D;
+  const int o_bytes = rows * D * 4;
+  if ((int64_t)span * (o_bytes + rows * 8) > scratch_bytes) {
+    const int warp = tid >> 5;
+    for (int t = warp; t < rows; t += nthreads / 32)
+      merge_segment_row(p, seg, HB, G, t / G, t - (t / G) * G, c0, span, U, n, D, out + (int64_t)t * D);
+    return;
+  }
+  float* so = reinterpret_cast<float*>(scratch);                            // [span][rows][D]
+  float2* sml = reinterpret_cast<float2*>(scratch + (size_t)span * o_bytes);  // [span][rows]
+  const bool some_empty = U < n;
+  // flat loops over (part, chunk) and (part, row): every copy and load of a
+  // thread is independent, so all are in flight at once
+  const int chunks = o_bytes / 16;  // 16-byte chunks of one part's rows
+  const uint32_t so_u32 = smem_u32(so);
+  for (int i = tid; i < span * chunks; i += nthreads) {
+    const int q = i / chunks, k = i - q * chunks;
+    if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
+    cp_async_16(so_u32 + (uint32_t)i * 16u, p.part_o + ((seg + c0 + q) * HB * G) * D + 4 * k, 16);
+  }
+#pragma unroll 4
+  for (int i = tid; i < span * rows; i += nthreads) {
+    const int q = i / rows, r = i - q * rows;
+    sml[i] = (some_empty && cta_range_empty(c0 + q, U, n)) ? make_float2(-INFINITY, 0.f)
+                                                          : __ldcg(p.part_ml + (seg + c0 + q) * HB * G + r);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  named_barrier(2, nthreads);
+  for (int x = tid; x < rows * (D / 4); x += nthreads) {
+    const int r = x / (D / 4), c4 = x - r * (D / 4);
+    float M = -INFINITY;
+    for (int q = 0; q < span; ++q) M = fmaxf(M, sml[q * rows + r].x);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < span; ++q) {
+      const float2 ml = sml[q * rows + r];
+      if (ml.x == -INFINITY) continue;
+      const float f = fast_exp2(ml.x - M);
+      const float4 v = reinterpret_cast<const float4*>(so + ((size_t)q * rows + r) * D)[c4];
+      den += f * ml.y;
+      acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+    }
+    const float inv = den > 0.f ? p.v_scale / den : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(out + (int64_t)r * D + 4 * c4) = packed;
+  }
+}
+
 // Compile-time shape of one configuration: HB heads per box, RT row tiles.
 template <int D, int HB, int RT, bool KV8 = false>
 struct Cfg {
@@ -113,12 +270,12 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
-  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + merge + prefix + 128 + 1024;
+  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 64 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
   if (s > kMaxStages) s = kMaxStages;
   L.stages = s;
   L.bar_off = s * C::kStageBytes + 2 * L.qslot;
-  L.mrg_off = L.bar_off + (2 * s + 4) * 8;
+  L.mrg_off = L.bar_off + (2 * s + 4) * 8 + 64;  // + the pending-merge list
   L.prefix_off = L.mrg_off + merge;
   L.total = L.prefix_off + prefix + 1024;
   return L;
@@ -150,6 +307,10 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [NBS][HB][G][D]
   float* mrg_ml = mrg_o + NBS * HB * G * D;                           // [NBS][HB][G][2]
   int* prefix = reinterpret_cast<int*>(smem + lay.prefix_off);        // [B+1] 16-key blocks before b
+  // segments this CTA merges after its range: [0] = count, then 4 ints each
+  // (b, head box, c0, span); bytes 48..55 hold this launch's counter tag
+  volatile int* pending = reinterpret_cast<volatile int*>(smem + lay.bar_off + (2 * S + 4) * 8);  // [16]
+  volatile unsigned long long* tag_slot = reinterpret_cast<volatile unsigned long long*>(pending + 12);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
@@ -192,7 +353,24 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   const int n = p.num_ctas, c = blockIdx.x;
   const int64_t u0 = (int64_t)c * U / n, u1 = (int64_t)(c + 1) * U / n;
   griddep_launch_dependents();
-  if (warp < C::kConsumers) griddep_wait();  // before any output write
+  // Counter tag of this launch, kept by thread 0 (the only thread that counts
+  // arrivals) in shared memory: read the epoch E, then count this CTA on the grid counter; the
+  // n-th CTA (every CTA has read E by then) stores E + 1.  The tag is the top
+  // 48 bits of (E + 1) times an odd constant (the 64-bit golden-ratio
+  // multiplier), so memory filled with a repeated byte or word does not read
+  // as a matching tag, and E and E + 1 give different tags.
+  if (warp < C::kConsumers) {
+    griddep_wait();  // before any output write, and before the epoch is read
+    if (tid == 0) {
+      pending[0] = 0;
+      const unsigned long long e = *reinterpret_cast<volatile unsigned long long*>(p.launch_epoch);
+      const unsigned long long tag = ((e + 1) * 0x9E3779B97F4A7C15ull) >> 16;
+      *tag_slot = tag;
+      __threadfence();
+      if (arrive_part(p.launch_epoch + 1, tag, p.err) == (unsigned)(n - 1))
+        *reinterpret_cast<volatile unsigned long long*>(p.launch_epoch) = e + 1;
+    }
+  }
   // sequences with no key (seq_len 0) get out = 0; CTA b % n writes them
   for (int b = c; b < B; b += n) {
     if (prefix[b + 1] != prefix[b]) continue;
@@ -658,16 +836,52 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       }
       named_barrier(1, C::kConsumers * 32);
     }
+    if (!complete && p.pre_chunks == 0) {
+      // This CTA's part of a segment cut across CTAs is written.  Publish and
+      // count it: the consumer barrier orders every consumer thread's partial
+      // writes before thread 0's fence (cumulative) and count.  The CTA that
+      // counts a segment's last part records it and merges it after its own
+      // range, with the stage ring idle; no other consumer waits on the count.
+      named_barrier(2, C::kConsumers * 32);
+      if (tid == 0) {
+        const int64_t us = (int64_t)Hg * prefix[cc.b] + (int64_t)cc.hk * cc.nblk;
+        const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(us + cc.nblk - 1, U, n);
+        int arrivals = c1 - c0 + 1;  // CTAs c0 .. c1 own the segment's units ...
+        if (U < n) {                 // ... except those without a unit, which took no part
+          arrivals = 0;
+          for (int x = c0; x <= c1; ++x) arrivals += cta_range_empty(x, U, n) ? 0 : 1;
+        }
+        __threadfence();
+        if (arrive_part(p.seg_count + seg_id, *tag_slot, p.err) == (unsigned)(arrivals - 1)) {
+          __threadfence();  // the other parts' partials before this CTA's merge reads them
+          const int e = pending[0];  // a CTA range cuts at most 2 segments
+          pending[1 + 4 * e] = cc.b;
+          pending[2 + 4 * e] = cc.hk;
+          pending[3 + 4 * e] = c0;
+          pending[4 + 4 * e] = c1 - c0 + 1;  // the merge walks the CTA span (empty CTAs weigh 0)
+          pending[0] = e + 1;
+        }
+      }
+    }
     advance(cc, seg_blocks);
+  }
+  if (p.pre_chunks == 0) {
+    named_barrier(2, C::kConsumers * 32);  // every count of this CTA recorded; the ring is idle
+    const int npend = pending[0];
+    for (int e = 0; e < npend; ++e) {
+      merge_segment<D>(p, pending[1 + 4 * e], pending[2 + 4 * e], pending[3 + 4 * e], pending[4 + 4 * e], HB, Hg,
+                       U, n, ring, S * C::kStageBytes, tid, C::kConsumers * 32);
+      named_barrier(2, C::kConsumers * 32);  // before the next merge reuses the ring
+    }
   }
 }
 
-// Merge the partials of (sequence, KV head) pairs that were cut across CTAs.
-// One CTA per pair; warp w merges rows g = w, w + 4, ... of the pair's G query
-// heads: lanes load the partials' (m, l) in parallel and reduce with
-// shuffles, then each lane accumulates 4 dims with float4 loads, all partials
-// in flight at once (a per-element loop over partials is a chain of dependent
-// loads: ~40 us at batch 32).
+// Cascade decode: merge each (sequence, KV head) pair's own-key partials
+// (those of every CTA that owns a part of the sequence; none if it has no key
+// of its own) with the shared prefix's partials, one per key chunk.  One CTA
+// per pair; warp w merges rows g = w, w + 4, ... of the pair's G query heads:
+// lanes load the partials' (m, l) in parallel and reduce with shuffles, then
+// each lane accumulates 4 dims with float4 loads, 8 partials in flight.
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int D) {
   const int Hkv = p.pool.num_kv_heads;
   const int HB = p.heads_per_box;
@@ -698,148 +912,74 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
   total = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   const int nblk = (seq_len_of(p, b, max_len) + 15) >> 4;
   griddep_wait();
-  if (p.pre_chunks > 0) {
-    // cascade: the pair's own-key partials (none if the sequence has no key of
-    // its own) merged with the shared prefix's partials, one per key chunk
-    const int n = p.num_ctas;
-    int c0 = 0, nparts = 0;
-    bool some_empty = false;
-    int64_t U = 0;
-    if (nblk > 0) {
-      U = total * Hg;
-      const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
-      c0 = cta_of_unit(us, U, n);
-      nparts = cta_of_unit(ue - 1, U, n) - c0 + 1;
-      some_empty = U < n;
-    }
-    const int64_t seg = (int64_t)b * Hg + hg;
-    const int nparts_all = nparts + p.pre_chunks;
-    const int64_t Hq = p.num_q_heads;
-    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hk * G) * D;
-    for (int g = warp; g < G; g += 4) {
-      const int64_t hq = (int64_t)hk * G + g;
-      auto ml_of = [&](int q) {  // q < nparts: own-key partial q; else prefix chunk q - nparts
-        if (q < nparts) {
-          if (some_empty && cta_range_empty(c0 + q, U, n)) return make_float2(-INFINITY, 0.f);
-          return __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
-        }
-        return __ldcg(p.pre_ml + ((int64_t)(q - nparts) * p.batch + b) * Hq + hq);
-      };
-      auto row_of = [&](int q) {
-        if (q < nparts)
-          return reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D);
-        return reinterpret_cast<const float4*>(p.pre_o + (((int64_t)(q - nparts) * p.batch + b) * Hq + hq) * D);
-      };
-      // (m, l): lane q holds partial q (the first 32), later ones are looped over
-      const float2 ml_mine = lane < nparts_all ? ml_of(lane) : make_float2(-INFINITY, 0.f);
-      float M = ml_mine.x;
-      for (int q = lane + 32; q < nparts_all; q += 32) M = fmaxf(M, ml_of(q).x);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float f_mine = (ml_mine.x == -INFINITY) ? 0.f : fast_exp2(ml_mine.x - M);
-      float den = f_mine * ml_mine.y;
-      for (int q = lane + 32; q < nparts_all; q += 32) {
-        const float2 ml = ml_of(q);
-        den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      const float inv = den > 0.f ? p.v_scale / den : 0.f;
-      // weighted rows, 8 partials at a time with all their loads in flight; a
-      // partial of weight 0 (empty, or negligible) is not read
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      const bool dims = 4 * lane < D;
-      for (int q0 = 0; q0 < nparts_all; q0 += 8) {
-        float f[8];
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q = q0 + u;
-          f[u] = __shfl_sync(0xffffffffu, f_mine, q & 31);
-          if (q >= 32 && q < nparts_all) {
-            const float2 ml = ml_of(q);
-            f[u] = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-          }
-          if (q >= nparts_all) f[u] = 0.f;
-          v[u] = (dims && f[u] != 0.f) ? __ldcg(row_of(q) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          acc.x += f[u] * v[u].x; acc.y += f[u] * v[u].y; acc.z += f[u] * v[u].z; acc.w += f[u] * v[u].w;
-        }
-      }
-      if (dims) {
-        uint2 packed;
-        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(outp + (int64_t)g * D + 4 * lane) = packed;
-      }
-    }
-    return;
-  }
-  if (nblk == 0) return;  // zeroed by the split kernel
-  const int64_t U = total * Hg;
   const int n = p.num_ctas;
-  const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
-  const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(ue - 1, U, n);
-  if (c0 == c1) return;  // written by the split kernel
-  const int nparts = c1 - c0 + 1;
-  const bool some_empty = U < n;  // only then can a CTA own no unit (and write no partial)
+  int c0 = 0, nparts = 0;
+  bool some_empty = false;
+  int64_t U = 0;
+  if (nblk > 0) {
+    U = total * Hg;
+    const int64_t us = before * Hg + (int64_t)hg * nblk, ue = us + nblk;
+    c0 = cta_of_unit(us, U, n);
+    nparts = cta_of_unit(ue - 1, U, n) - c0 + 1;
+    some_empty = U < n;
+  }
   const int64_t seg = (int64_t)b * Hg + hg;
-  __nv_bfloat16* outp =
-      static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * p.num_q_heads + (int64_t)hk * G) * D;
-  constexpr int kRegParts = 8;  // partial rows held in registers (one load round trip)
+  const int nparts_all = nparts + p.pre_chunks;
+  const int64_t Hq = p.num_q_heads;
+  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hk * G) * D;
   for (int g = warp; g < G; g += 4) {
-    // One round trip when nparts <= kRegParts: every lane loads its (m, l) (lane
-    // q = partial q) and its four dims of every partial row at once; the weights
-    // come from the warp max and are broadcast by shuffles.
-    float4 vr[kRegParts];
-    const bool dims = 4 * lane < D;
-#pragma unroll
-    for (int q = 0; q < kRegParts; ++q) {
-      vr[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (q < nparts && dims && !(some_empty && cta_range_empty(c0 + q, U, n)))
-        vr[q] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D) + lane);
-    }
-    float2 ml_mine = make_float2(-INFINITY, 0.f);  // (m, l) of partial `lane`
-    if (lane < nparts && !(some_empty && cta_range_empty(c0 + lane, U, n)))
-      ml_mine = __ldcg(p.part_ml + ((seg + c0 + lane) * HB + h) * G + g);
+    const int64_t hq = (int64_t)hk * G + g;
+    auto ml_of = [&](int q) {  // q < nparts: own-key partial q; else prefix chunk q - nparts
+      if (q < nparts) {
+        if (some_empty && cta_range_empty(c0 + q, U, n)) return make_float2(-INFINITY, 0.f);
+        return __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
+      }
+      return __ldcg(p.pre_ml + ((int64_t)(q - nparts) * p.batch + b) * Hq + hq);
+    };
+    auto row_of = [&](int q) {
+      if (q < nparts)
+        return reinterpret_cast<const float4*>(p.part_o + (((seg + c0 + q) * HB + h) * G + g) * D);
+      return reinterpret_cast<const float4*>(p.pre_o + (((int64_t)(q - nparts) * p.batch + b) * Hq + hq) * D);
+    };
+    // (m, l): lane q holds partial q (the first 32), later ones are looped over
+    const float2 ml_mine = lane < nparts_all ? ml_of(lane) : make_float2(-INFINITY, 0.f);
     float M = ml_mine.x;
-    for (int q = lane + 32; q < nparts; q += 32) {
-      if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
-      M = fmaxf(M, __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g).x);
-    }
+    for (int q = lane + 32; q < nparts_all; q += 32) M = fmaxf(M, ml_of(q).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float f_mine = (ml_mine.x == -INFINITY) ? 0.f : fast_exp2(ml_mine.x - M);
     float den = f_mine * ml_mine.y;
-    for (int q = lane + 32; q < nparts; q += 32) {
-      if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
-      const float2 ml = __ldcg(p.part_ml + ((seg + c0 + q) * HB + h) * G + g);
+    for (int q = lane + 32; q < nparts_all; q += 32) {
+      const float2 ml = ml_of(q);
       den += (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M) * ml.y;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? p.v_scale / den : 0.f;
-    // weighted sum of the partial rows: lane owns dims 4*lane .. 4*lane+3 (D <= 128)
+    // weighted rows, 8 partials at a time with all their loads in flight; a
+    // partial of weight 0 (empty, or negligible) is not read
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool dims = 4 * lane < D;
+    for (int q0 = 0; q0 < nparts_all; q0 += 8) {
+      float f[8];
+      float4 v[8];
 #pragma unroll
-    for (int q = 0; q < kRegParts; ++q) {
-      const float f = __shfl_sync(0xffffffffu, f_mine, q);
-      if (q < nparts) {
-        acc.x += f * vr[q].x; acc.y += f * vr[q].y; acc.z += f * vr[q].z; acc.w += f * vr[q].w;
+      for (int u = 0; u < 8; ++u) {
+        const int q = q0 + u;
+        f[u] = __shfl_sync(0xffffffffu, f_mine, q & 31);
+        if (q >= 32 && q < nparts_all) {
+          const float2 ml = ml_of(q);
+          f[u] = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+        }
+        if (q >= nparts_all) f[u] = 0.f;
+        v[u] = (dims && f[u] != 0.f) ? __ldcg(row_of(q) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x += f[u] * v[u].x; acc.y += f[u] * v[u].y; acc.z += f[u] * v[u].z; acc.w += f[u] * v[u].w;
       }
     }
     if (dims) {
-#pragma unroll 4
-      for (int q = kRegParts; q < nparts; ++q) {
-        if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
-        const int64_t sidx = (seg + c0 + q) * HB + h;
-        const float mq = __ldcg(p.part_ml + sidx * G + g).x;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sidx * G + g) * D) + lane);
-        const float f = (mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
-        acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
-      }
       uint2 packed;
       packed.x = pack_bf16(acc.x * inv, acc.y * inv);
       packed.y = pack_bf16(acc.z * inv, acc.w * inv);
@@ -948,9 +1088,8 @@ cudaError_t launch_split_only(const DecodeParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
-  cudaError_t e = launch_split_only(p, s);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(decode_combine_kernel, dim3(p.batch * p.pool.num_kv_heads), dim3(128), 0, s, p, p.pool.head_dim);
+  // segments cut across CTAs are merged inside the split kernel
+  return launch_split_only(p, s);
 }
 
 

@@ -17,7 +17,7 @@
 // kernels overlap on the GPU (on different streams, or on one device from
 // several host threads without ordering) race on it.  Nothing in it needs to
 // start zeroed: every partial a call reads is written earlier in the same
-// call, by the split kernel that the combine kernel follows on the stream.
+// launch, and the arrival counters carry the launch's grid id.
 #include <atomic>
 
 #include "../../include/paged_attn.h"

@@ -47,6 +47,16 @@ struct DecodeParams {
   int64_t kv_len;                  // CSR form: entries of kv_indices
   float* part_o;          // [slots, G, D] fp32 unnormalised partial outputs
   float2* part_ml;        // [slots, G] (running max in log2 units, denominator)
+  // launch epoch word + grid arrival counter (2 words at a fixed place, the
+  // workspace's start): every launch reads the epoch E, and the last of its
+  // CTAs to have read it stores E + 1, so E differs between consecutive
+  // launches on one workspace (CUDA graph replays included) whatever the
+  // words held before
+  unsigned long long* launch_epoch;
+  // [B * Hkv] arrival counters of segments cut across CTAs, tagged with E
+  // (any other contents read as zero): the last CTA to finish its part of a
+  // segment merges the segment's partials
+  unsigned long long* seg_count;
   int32_t heads_per_box;  // HB: KV heads loaded per TMA box (power of two <= 8)
   int32_t smem_budget;    // dynamic shared memory the stage ring is sized against
   int32_t batch;

@@ -1,0 +1,143 @@
+"""GPU checks of the split-KV merge inside the decode kernel.
+
+A segment (one sequence's keys for one box of KV heads) whose 16-key blocks
+are cut across CTAs is finished by whichever CTA completes its last part: the
+CTAs count their parts in workspace words tagged with the launch's grid id,
+and the last one merges every part's (m, l, o) with the combine identity
+(mobius PR #395 "Add paged / block-table KV cache export": the decode output
+is softmax attention over all seq_lens[b] keys, which the merge reassembles
+exactly up to rounding).  So the workspace needs no initialisation, and every
+launch -- eager or a CUDA graph replay -- must merge afresh.  Each case below
+changes the inputs between launches, so a launch that skipped its merge would
+leave a stale or zero output and fail against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from serving_slot_mapping_gb300 import build as build_mod
+from serving_slot_mapping_gb300 import capi
+from serving_slot_mapping_gb300 import workloads as wl
+
+from _parity import assert_close, bits, gpu_step, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    build_mod.build()
+    capi.lib()
+    capi.device_error()  # clear
+
+
+def _appended(plan, device):
+    st = wl.materialize(plan, device)
+    kp, vp, _ = gpu_step(st)
+    return st, kp, vp
+
+
+def _expect(st, kp, vp, q):
+    p = st.plan
+    return oracle.paged_attention_decode(to_f64(bits(kp)), to_f64(bits(vp)), to_f64(bits(q)),
+                                         p.block_table, p.seq_lens, p.scale)
+
+
+def _new_q(q, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(q.shape, generator=g).to(q.dtype).to(q.device)
+
+
+def _decode(st, kp, vp, q, ws, out=None, stream=None):
+    p = st.plan
+    if out is None:  # NaN until written: a row the kernel skipped cannot pass
+        out = torch.full_like(q, float("nan"))
+    return capi.paged_attention_decode(kp, vp, q, st.block_table, st.seq_lens, p.scale,
+                                       max_seq_len=int(p.seq_lens.max()), out=out, workspace=ws,
+                                       stream=stream)
+
+
+@pytest.mark.parametrize("fill", ["zeros", "ones", "pattern", "random"])
+def test_merge_with_uninitialised_workspace(cuda_device, fill):
+    plan = wl.gqa_decode_plan()  # 32 sequences of 512..4096 keys: most cut across CTAs
+    st, kp, vp = _appended(plan, cuda_device)
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+    if fill == "zeros":
+        ws.zero_()
+    elif fill == "ones":
+        ws.fill_(0xFF)
+    elif fill == "pattern":
+        ws.fill_(0x5A)
+    else:
+        ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, generator=torch.Generator().manual_seed(7)))
+    out = _decode(st, kp, vp, st.q, ws)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    assert_close(out, _expect(st, kp, vp, st.q), "bf16", f"merge, workspace {fill}")
+
+
+def test_merge_repeated_calls_and_shapes_share_one_workspace(cuda_device):
+    big = wl.gqa_decode_plan()
+    small = wl.gqa_decode_plan(batch=5, lo=300, hi=6000, seed=9)
+    mqa = wl.long_context_plan(hkv=1, batch=6, lo=1000, hi=9000, seed=13)  # 32 rows per KV head
+    rigs = [_appended(p, cuda_device) for p in (big, small, mqa)]
+    ws = capi.decode_workspace(big.batch, big.num_q_heads, rigs[0][1])
+    for p, (st, kp, vp) in zip((big, small, mqa), rigs):
+        need = capi.decode_workspace_size(p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim)
+        assert need <= ws.numel()
+    for rep in range(2):
+        for i, (st, kp, vp) in enumerate(rigs):
+            q = _new_q(st.q, 100 * rep + i)
+            out = _decode(st, kp, vp, q, ws)
+            torch.cuda.synchronize()
+            assert capi.device_error() == (0, 0)
+            assert_close(out, _expect(st, kp, vp, q), "bf16", f"merge rep {rep} plan {i}")
+
+
+def test_merge_in_cuda_graph_replays(cuda_device):
+    plan = wl.gqa_decode_plan(batch=16, seed=5)
+    st, kp, vp = _appended(plan, cuda_device)
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+    q = st.q.clone()
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _decode(st, kp, vp, q, ws, out=out, stream=s)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _decode(st, kp, vp, q, ws, out=out, stream=s)
+    for rep in range(4):
+        qn = _new_q(q, 1000 + rep)
+        q.copy_(qn)
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        assert_close(out, _expect(st, kp, vp, qn), "bf16", f"graph replay {rep}")
+
+
+def test_merge_e4m3_pools(cuda_device):
+    plan = wl.long_context_plan(hkv=8, batch=8, lo=2000, hi=12000, seed=17)
+    st, kp, vp = _appended(plan, cuda_device)
+    ks, vs = 0.02, 0.03
+    from oracle import kv_fp8
+    kc = kv_fp8.quantize(to_f64(bits(kp)), ks)
+    vc = kv_fp8.quantize(to_f64(bits(vp)), vs)
+    kp8 = torch.from_numpy(kc).to(cuda_device).view(torch.float8_e4m3fn)
+    vp8 = torch.from_numpy(vc).to(cuda_device).view(torch.float8_e4m3fn)
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp8)
+    ws.fill_(0xA5)
+    for rep in range(2):
+        q = _new_q(st.q, 50 + rep)
+        out = torch.full_like(q, float("nan"))
+        capi.paged_attention_decode(kp8, vp8, q, st.block_table, st.seq_lens, plan.scale,
+                                    max_seq_len=int(plan.seq_lens.max()), out=out, workspace=ws,
+                                    k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        exp = kv_fp8.paged_attention_decode_fp8(kc, vc, ks, vs, to_f64(bits(q)), plan.block_table,
+                                                plan.seq_lens, plan.scale)
+        assert_close(out, exp, "bf16", f"e4m3 merge rep {rep}")
