@@ -268,6 +268,14 @@ class DecodeRig:
         self.append()
         self.decode()
 
+    def fused_step(self):
+        """The same step as one call (one launch): append + decode."""
+        st = self.st
+        self.capi.paged_attention_decode_append(st.key_pool, st.value_pool, st.key, st.value,
+                                                st.slot_mapping, st.q, st.block_table, st.seq_lens,
+                                                self.plan.scale, max_seq_len=self.msl, out=self.out,
+                                                workspace=self.ws)
+
 
 class PrefillRig:
     def __init__(self, plan, dev):
@@ -610,6 +618,23 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
             torch.cuda.empty_cache()
         except Exception as ex:
             res[name + "_fp8"] = {"error": repr(ex)[:200]}
+    for name in ["gqa_decode", "long_gqa"]:  # append + decode as one call vs two
+        try:
+            plan = wl.named_plan(name)
+            rig = DecodeRig(plan, dev)
+            g2 = capture(rig.step, stream)
+            g1 = capture(rig.fused_step, stream)
+            ms2 = statistics.mean(timed_graph(g2, steps, flush, stream))
+            ms1 = statistics.mean(timed_graph(g1, steps, flush, stream))
+            kvb = wl.decode_kv_bytes(plan)
+            res[name + "_fused_step"] = {"step_ms": round(ms1, 5), "two_call_step_ms": round(ms2, 5),
+                                         "kv_GBps": round(kvb / (ms1 * 1e-3) / 1e9, 1),
+                                         "frac_hbm": round(kvb / (ms1 * 1e-3) / 1e9 / hbm, 4),
+                                         "speedup_vs_two_calls": round(ms2 / ms1, 3)}
+            del rig, g1, g2
+            torch.cuda.empty_cache()
+        except Exception as ex:
+            res[name + "_fused_step"] = {"error": repr(ex)[:200]}
     try:  # the GQA decode batch with its page table in CSR form
         plan = wl.named_plan("gqa_decode")
         rig = DecodeRig(plan, dev)

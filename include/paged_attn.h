@@ -236,6 +236,39 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_attention_decode_append -- one decode step in one launch: the append
+ * of this step's K/V rows (paged_kv_append with one token per sequence) and
+ * the decode that attends to them (mobius PR #395, "How it works (per
+ * attention layer)": step 1 writes the new rows, step 2 attends).  The
+ * result equals paged_kv_append(pool, key, value, slot_mapping, batch)
+ * followed by paged_attention_decode(...) with the same arguments, provided
+ *   (a) slot_mapping[b] >= 0 is the slot of sequence b's last key, position
+ *       seq_lens[b] - 1 (block_table[b][(L-1)/page_size] * page_size +
+ *       (L-1) % page_size) -- the new token of a decode step; and
+ *   (b) no slot written by the call is a key of another sequence.
+ * The new rows are written to the pool and, for each sequence, attended to
+ * straight from key/value (the pool row is not read back).  An entry
+ * breaking (a) is recorded in the device error word (code 2, detail = the
+ * slot) and that sequence's output then attends to the new row in place of
+ * its last key.  slot_mapping[b] < 0: sequence b has no new token (its keys
+ * are all in the pool already).
+ *
+ * key, value    device [batch, num_kv_heads, head_dim] bf16 (f32 for f32
+ *               pools), 16-byte aligned; e4m3 pools store their codes
+ *               (quantised as paged_kv_append does).
+ * slot_mapping  device int64 [batch], 8-byte aligned.
+ * Every other argument, limit and the workspace are those of
+ * paged_attention_decode.  f32 pools run the append and the decode as two
+ * launches.
+ */
+pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key, const void* value,
+                                        const int64_t* slot_mapping, const void* q, void* out,
+                                        int32_t batch, int32_t num_q_heads,
+                                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace.  The pages have no counterpart of this call: it
  * exists for callers that cannot allocate device memory, such as a plugin in

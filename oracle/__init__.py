@@ -30,7 +30,10 @@ What it follows:
   quantising append and decode over the values the codes stand for;
 * the compressed (CSR) page-table form ``kv_indptr`` / ``kv_indices`` /
   ``kv_last_page_len`` named by NVIDIA/recsys-examples PR #400
-  (KVCacheMetadata).
+  (KVCacheMetadata);
+* one decode step as one call: the append of the step's rows followed by
+  the decode that attends to them (mobius page, "How it works (per
+  attention layer)", steps 1 and 2).
 
 Readings where the pages are silent are listed in the module docstring of
 :mod:`oracle.paged_attention`.
@@ -49,6 +52,7 @@ from .paged_attention import (  # noqa: F401
     paged_attention_prefill,
     paged_attention_decode_partial,
     paged_attention_decode_cascade,
+    paged_attention_decode_append,
     csr_pages,
     paged_attention_decode_csr,
     paged_attention_prefill_csr,

@@ -115,3 +115,13 @@ def paged_attention_decode_fp8(key_codes, value_codes, k_scale, v_scale, q, bloc
     """Decode over e4m3 pools: the plain decode on the values the codes stand for."""
     return paged_attention_decode(dequantize(key_codes, k_scale), dequantize(value_codes, v_scale), q,
                                   block_table, seq_lens, scale, seqs=seqs)
+
+
+def paged_attention_decode_append_fp8(key_codes, value_codes, key, value, slot_mapping, k_scale, v_scale,
+                                      q, block_table, seq_lens, scale, seqs=None):
+    """One decode step on e4m3 pools as one call: the quantising append of
+    this step's rows, then decode over the values the codes stand for.
+    Returns ``(key_codes', value_codes', out)``."""
+    kc, vc = paged_kv_append_fp8(key_codes, value_codes, key, value, slot_mapping, k_scale, v_scale)
+    return kc, vc, paged_attention_decode_fp8(kc, vc, k_scale, v_scale, q, block_table, seq_lens, scale,
+                                              seqs=seqs)

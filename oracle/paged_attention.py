@@ -191,6 +191,17 @@ def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale
     return out
 
 
+def paged_attention_decode_append(key_pool, value_pool, key, value, slot_mapping, q, block_table,
+                                  seq_lens, scale, seqs=None):
+    """One decode step as one call: this step's K/V rows ``key/value [B, Hkv, D]``
+    are appended at ``slot_mapping [B]`` (step 1 of mobius PR #395, "How it
+    works (per attention layer)"), then every sequence attends over the
+    updated pools with ``seq_lens`` that count the new token (step 2).
+    Returns ``(key_pool', value_pool', out)``."""
+    kp, vp = paged_kv_append(key_pool, value_pool, key, value, slot_mapping)
+    return kp, vp, paged_attention_decode(kp, vp, q, block_table, seq_lens, scale, seqs=seqs)
+
+
 def paged_attention_decode_partial(key_pool, value_pool, q, block_table, seq_lens, scale,
                                    key_ranges):
     """Decode partials over key ranges ``key_ranges[b] = (lo, hi)`` (fp64).

@@ -20,9 +20,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "prefill_bf16.cu", "attn_f32.cu",
+SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_fused.cu", "prefill_bf16.cu", "attn_f32.cu",
            "decode_noalloc.cu", "tmap.cu"]
-HEADERS = ["common.cuh", "internal.h", "tma.cuh", "tcgen05.cuh"]
+HEADERS = ["common.cuh", "internal.h", "tma.cuh", "tcgen05.cuh", "decode_split.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

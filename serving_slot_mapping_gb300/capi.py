@@ -47,6 +47,9 @@ SIGNATURES = {
     "paged_attention_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "paged_attention_decode": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i32,
                                       _c_void_p, _i32, _f32, _c_void_p, _sz, _c_void_p]),
+    "paged_attention_decode_append": (_i32, [_PPOOL, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                             _c_void_p, _i32, _i32, _c_void_p, _i32, _c_void_p, _i32,
+                                             _f32, _c_void_p, _sz, _c_void_p]),
     "paged_attention_decode_static_scratch": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32,
                                                      _c_void_p, _i32, _c_void_p, _i32, _f32,
                                                      _c_void_p]),
@@ -202,6 +205,42 @@ def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale
                                       _ptr(block_table), mb, _ptr(seq_lens), int(max_seq_len),
                                       float(scale), _ptr(workspace), wbytes, _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_append(key_pool, value_pool, key, value, slot_mapping, q, block_table,
+                                  seq_lens, scale, max_seq_len=None, out=None, workspace=None,
+                                  stream=None, k_scale=1.0, v_scale=1.0):
+    """One decode step in one launch: append ``key/value [B, Hkv, D]`` at
+    ``slot_mapping`` int64 [B] (each the slot of its sequence's last key, or
+    < 0 for none), then decode ``q [B, Hq, D]`` over the updated pools
+    (``seq_lens`` count the new token).  Returns ``out``; the pools are
+    updated in place."""
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
+    for t, nm in ((q, "q"), (block_table, "block_table"), (key, "key"), (value, "value"),
+                  (slot_mapping, "slot_mapping")):
+        _contig(t, nm)
+    B, hq, d = q.shape
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if key.shape[0] != B or value.shape[0] != B or slot_mapping.numel() != B:
+        raise ValueError("one new token per sequence: key/value [B, Hkv, D], slot_mapping [B]")
+    mb = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = mb * pool.page_size
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, hq, key_pool)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_attention_decode_append(ctypes.byref(pool), _ptr(key), _ptr(value),
+                                             _ptr(slot_mapping), _ptr(q), _ptr(out), B, hq,
+                                             _ptr(block_table), mb, _ptr(seq_lens),
+                                             int(max_seq_len), float(scale), _ptr(workspace), wbytes,
+                                             _stream(stream))
+    _check(st, "paged_attention_decode_append")
     return out
 
 

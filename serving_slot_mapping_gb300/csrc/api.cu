@@ -440,6 +440,39 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
                      max_seq_len, scale, workspace, workspace_bytes, stream);
 }
 
+pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key, const void* value,
+                                        const int64_t* slot_mapping, const void* q, void* out, int32_t batch,
+                                        int32_t num_q_heads, const int32_t* block_table,
+                                        int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                        int32_t max_seq_len, float scale, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  const Table t = dense_table(block_table, max_blocks_per_seq, seq_lens);
+  pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (batch == 0) return PA_OK;
+  if (q == nullptr || out == nullptr || key == nullptr || value == nullptr || slot_mapping == nullptr)
+    return PA_ERR_NULL;
+  st = check_table(t);
+  if (st != PA_OK) return st;
+  if (q == out) return PA_ERR_SHAPE;
+  if (!aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
+  if (pool->dtype == PA_DTYPE_F32) {  // the f32 path: append and decode as two launches
+    st = paged_kv_append(pool, key, value, slot_mapping, batch, stream);
+    if (st != PA_OK) return st;
+    return decode_impl(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, stream);
+  }
+  if (!aligned(key, 16) || !aligned(value, 16)) return PA_ERR_ALIGN;  // 8 bf16 elements per access
+  pa::DecodeParams p;
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, &p);
+  if (st != PA_OK) return st;
+  p.new_k = key;
+  p.new_v = value;
+  p.new_slots = slot_mapping;
+  p.k_quant = kv8(pool) ? pool->k_scale : 1.f;
+  p.v_quant = kv8(pool) ? pool->v_scale : 1.f;
+  return pa::launch_decode_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status paged_attention_decode_csr(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
                                      int32_t num_q_heads, const int32_t* kv_indptr, const int32_t* kv_indices,
                                      int64_t num_kv_indices, const int32_t* kv_last_page_len,

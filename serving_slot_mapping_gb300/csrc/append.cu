@@ -53,18 +53,6 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   }
 }
 
-// e4m3 pools: eight bf16 elements (one 16-byte load) become eight codes (one
-// 8-byte store); code = e4m3_rn_satfinite(x / scale) with an IEEE division.
-__device__ __forceinline__ uint2 quantize8(uint4 v, float scale) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    c[j] = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[j] << 16), scale),
-                           __fdiv_rn(__uint_as_float(w[j] & 0xFFFF0000u), scale));
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
 __global__ void __launch_bounds__(256) append_e4m3_kernel(AppendParams p) {
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;

@@ -53,6 +53,15 @@ struct DecodeParams {
   // launches on one workspace (CUDA graph replays included) whatever the
   // words held before
   unsigned long long* launch_epoch;
+  // fused append + decode: this step's rows (bf16 [B, Hkv, D]) and their
+  // slots (int64 [B]); new_k == nullptr for a plain decode.  The kernel writes
+  // them to the pool (e4m3 pools: codes with k_quant / v_quant) and attends
+  // to each sequence's new row from the input, not from the pool.
+  const void* new_k;
+  const void* new_v;
+  const int64_t* new_slots;
+  float k_quant;
+  float v_quant;
   // [B * Hkv] arrival counters of segments cut across CTAs, tagged with E
   // (any other contents read as zero): the last CTA to finish its part of a
   // segment merges the segment's partials
@@ -81,6 +90,9 @@ struct DecodeParams {
 int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size);
 int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box);
 int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t heads_per_box);
+// Launch the fused (append + decode) split kernel (decode_fused.cu).
+cudaError_t launch_split_fused(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rt,
+                               cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 // Cascade: split kernel on s, then the combine after `prefix_done` (an event
 // recorded once the prefix partials are written) has completed.
