@@ -3,6 +3,8 @@
 // cascade decode only, the combine kernel that merges the split kernel's
 // partials with the shared prefix's.  The split kernel itself is in
 // decode_split.cuh (see there for the work decomposition).
+#include <atomic>
+
 #include "decode_split.cuh"
 
 namespace pa {
@@ -122,6 +124,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeParams p, int
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_coop_state{0};
+}  // namespace
+
+int coop_launch_state() { return g_coop_state.load(std::memory_order_relaxed); }
+void set_coop_launch_state(int v) { g_coop_state.store(v, std::memory_order_relaxed); }
 
 int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size) {
   const int rt = group <= 16 ? 1 : 2;

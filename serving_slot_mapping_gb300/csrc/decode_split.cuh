@@ -178,18 +178,23 @@ __device__ __noinline__ void merge_segment_row(const DecodeParams& p, int64_t se
 // Parts that do not fit in the ring are merged warp by warp from global memory.
 template <int D>
 __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb, int c0, int span, int HB, int Hg,
-                                           int64_t U, int n, unsigned char* scratch, int scratch_bytes, int tid,
-                                           int nthreads) {
+                                           int64_t U, int n, int row_lo, int row_hi, unsigned char* scratch,
+                                           int scratch_bytes, int tid, int nthreads) {
   const int G = p.group;
-  const int rows = HB * G;
+  const int all_rows = HB * G;  // a part's rows (h, g), contiguous
+  const int rows = row_hi - row_lo;  // the rows merged here
+  if (rows <= 0) return;
   const int64_t seg = (int64_t)b * Hg + hkb;
   const int64_t Hq = p.num_q_heads;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hkb * HB * G) * D;
+  __nv_bfloat16* out =
+      static_cast<__nv_bfloat16*>(p.out) + ((int64_t)b * Hq + (int64_t)hkb * HB * G + row_lo) * D;
   const int o_bytes = rows * D * 4;
   if ((int64_t)span * (o_bytes + rows * 8) > scratch_bytes) {
     const int warp = tid >> 5;
-    for (int t = warp; t < rows; t += nthreads / 32)
-      merge_segment_row(p, seg, HB, G, t / G, t - (t / G) * G, c0, span, U, n, D, out + (int64_t)t * D);
+    for (int t = warp; t < rows; t += nthreads / 32) {
+      const int r = row_lo + t;
+      merge_segment_row(p, seg, HB, G, r / G, r - (r / G) * G, c0, span, U, n, D, out + (int64_t)t * D);
+    }
     return;
   }
   float* so = reinterpret_cast<float*>(scratch);                            // [span][rows][D]
@@ -202,13 +207,13 @@ __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb
   for (int i = tid; i < span * chunks; i += nthreads) {
     const int q = i / chunks, k = i - q * chunks;
     if (some_empty && cta_range_empty(c0 + q, U, n)) continue;
-    cp_async_16(so_u32 + (uint32_t)i * 16u, p.part_o + ((seg + c0 + q) * HB * G) * D + 4 * k, 16);
+    cp_async_16(so_u32 + (uint32_t)i * 16u, p.part_o + ((seg + c0 + q) * all_rows + row_lo) * D + 4 * k, 16);
   }
 #pragma unroll 4
   for (int i = tid; i < span * rows; i += nthreads) {
     const int q = i / rows, r = i - q * rows;
     sml[i] = (some_empty && cta_range_empty(c0 + q, U, n)) ? make_float2(-INFINITY, 0.f)
-                                                          : __ldcg(p.part_ml + (seg + c0 + q) * HB * G + r);
+                                                          : __ldcg(p.part_ml + (seg + c0 + q) * all_rows + row_lo + r);
   }
   cp_async_commit();
   cp_async_wait<0>();
@@ -277,12 +282,12 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
-  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 64 + merge + prefix + 128 + 1024;
+  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 128 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
   if (s > kMaxStages) s = kMaxStages;
   L.stages = s;
   L.bar_off = s * C::kStageBytes + 2 * L.qslot;
-  L.mrg_off = L.bar_off + (2 * s + 4) * 8 + 64;  // + the pending-merge list
+  L.mrg_off = L.bar_off + (2 * s + 4) * 8 + 128;  // + the pending-merge list
   L.prefix_off = L.mrg_off + merge;
   L.total = L.prefix_off + prefix + 1024;
   return L;
@@ -314,10 +319,12 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [NBS][HB][G][D]
   float* mrg_ml = mrg_o + NBS * HB * G * D;                           // [NBS][HB][G][2]
   int* prefix = reinterpret_cast<int*>(smem + lay.prefix_off);        // [B+1] 16-key blocks before b
-  // segments this CTA merges after its range: [0] = count, then 4 ints each
-  // (b, head box, c0, span); bytes 48..55 hold this launch's counter tag
-  volatile int* pending = reinterpret_cast<volatile int*>(smem + lay.bar_off + (2 * S + 4) * 8);  // [16]
-  volatile unsigned long long* tag_slot = reinterpret_cast<volatile unsigned long long*>(pending + 12);
+  // segments this CTA merges (some of) after its range: [0] = count, then
+  // kPend ints each (b, head box, c0, span, parts, this CTA's part index);
+  // bytes 96..103 hold this launch's counter tag
+  constexpr int kPend = 6;
+  volatile int* pending = reinterpret_cast<volatile int*>(smem + lay.bar_off + (2 * S + 4) * 8);  // [24]
+  volatile unsigned long long* tag_slot = reinterpret_cast<volatile unsigned long long*>(pending + 24);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ps = p.pool.page_size, pshift = p.pool.page_shift;
@@ -911,26 +918,34 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     if (!complete && p.pre_chunks == 0) {
       // This CTA's part of a segment cut across CTAs is written.  Publish and
       // count it: the consumer barrier orders every consumer thread's partial
-      // writes before thread 0's fence (cumulative) and count.  The CTA that
-      // counts a segment's last part records it and merges it after its own
-      // range, with the stage ring idle; no other consumer waits on the count.
+      // writes before thread 0's fence (cumulative) and count.  The segment is
+      // merged after the CTAs' ranges, with the stage rings idle: by each CTA
+      // holding a part, a slice of the rows each (co-resident grid), or else by
+      // the CTA that counts the last part.  No consumer waits here.
       named_barrier(2, C::kConsumers * 32);
       if (tid == 0) {
         const int64_t us = (int64_t)Hg * prefix[cc.b] + (int64_t)cc.hk * cc.nblk;
         const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(us + cc.nblk - 1, U, n);
-        int arrivals = c1 - c0 + 1;  // CTAs c0 .. c1 own the segment's units ...
-        if (U < n) {                 // ... except those without a unit, which took no part
-          arrivals = 0;
-          for (int x = c0; x <= c1; ++x) arrivals += cta_range_empty(x, U, n) ? 0 : 1;
+        int arrivals = c1 - c0 + 1, mine = c - c0;  // CTAs c0 .. c1 own the segment's units ...
+        if (U < n) {  // ... except those without a unit, which took no part
+          arrivals = mine = 0;
+          for (int x = c0; x <= c1; ++x) {
+            const int part = cta_range_empty(x, U, n) ? 0 : 1;
+            arrivals += part;
+            if (x < c) mine += part;
+          }
         }
         __threadfence();
-        if (arrive_part(p.seg_count + seg_id, *tag_slot, p.err) == (unsigned)(arrivals - 1)) {
-          __threadfence();  // the other parts' partials before this CTA's merge reads them
+        const bool last = arrive_part(p.seg_count + seg_id, *tag_slot, p.err) == (unsigned)(arrivals - 1);
+        if (p.slice_merge || last) {
           const int e = pending[0];  // a CTA range cuts at most 2 segments
-          pending[1 + 4 * e] = cc.b;
-          pending[2 + 4 * e] = cc.hk;
-          pending[3 + 4 * e] = c0;
-          pending[4 + 4 * e] = c1 - c0 + 1;  // the merge walks the CTA span (empty CTAs weigh 0)
+          volatile int* ent = pending + 1 + kPend * e;
+          ent[0] = cc.b;
+          ent[1] = cc.hk;
+          ent[2] = c0;
+          ent[3] = c1 - c0 + 1;  // the merge walks the CTA span (empty CTAs weigh 0)
+          ent[4] = p.slice_merge ? arrivals : 1;
+          ent[5] = p.slice_merge ? mine : 0;
           pending[0] = e + 1;
         }
       }
@@ -941,12 +956,45 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     named_barrier(2, C::kConsumers * 32);  // every count of this CTA recorded; the ring is idle
     const int npend = pending[0];
     for (int e = 0; e < npend; ++e) {
-      merge_segment<D>(p, pending[1 + 4 * e], pending[2 + 4 * e], pending[3 + 4 * e], pending[4 + 4 * e], HB, Hg,
-                       U, n, ring, S * C::kStageBytes, tid, C::kConsumers * 32);
+      volatile int* ent = pending + 1 + kPend * e;
+      const int b = ent[0], hkb = ent[1], c0 = ent[2], span = ent[3], parts = ent[4], mine = ent[5];
+      if (p.slice_merge) {
+        // wait for the segment's last part (its CTAs are all resident and run
+        // to their range ends without waiting on anyone), then merge rows
+        // [mine, mine + 1) * rows / parts
+        if (tid == 0) {
+          const unsigned long long tag = *tag_slot;
+          const unsigned long long* cnt = p.seg_count + (int64_t)b * Hg + hkb;
+          const unsigned long long t0 = global_ns();
+          for (;;) {
+            const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(cnt);
+            if ((w >> 16) == tag && (int)(w & 0xFFFFu) >= parts) break;
+            if (global_ns() - t0 > kWaitLimitNs) {
+              record_error(p.err, ERR_TIMEOUT, -2);
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+      }
+      if (tid == 0) __threadfence();  // the other parts' partials before this CTA's merge reads them
+      named_barrier(2, C::kConsumers * 32);
+      const int rows = HB * p.group;
+      merge_segment<D>(p, b, hkb, c0, span, HB, Hg, U, n, mine * rows / parts, (mine + 1) * rows / parts, ring,
+                       S * C::kStageBytes, tid, C::kConsumers * 32);
       named_barrier(2, C::kConsumers * 32);  // before the next merge reuses the ring
     }
   }
 }
+
+}  // namespace
+
+// Cooperative launch with programmatic serialization: 0 not tried yet, 1
+// accepted, -1 refused (decode_bf16.cu).
+int coop_launch_state();
+void set_coop_launch_state(int v);
+
+namespace {
 
 template <int D, int HB, int RT, bool KV8, bool FUSED>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
@@ -956,6 +1004,27 @@ cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUt
   auto kern = decode_split_kernel<D, HB, RT, KV8, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
+  // Plain decode: a co-resident (cooperative) grid lets every CTA of a cut
+  // segment merge a slice of it.  Whether the runtime takes a cooperative
+  // launch with programmatic serialization is learnt from the first eager
+  // launch (never tried inside a stream capture); otherwise the CTA counting
+  // a segment's last part merges it whole.
+  if (p.pre_chunks == 0 && coop_launch_state() >= 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+        (cs == cudaStreamCaptureStatusNone || coop_launch_state() > 0)) {
+      DecodeParams pc = p;
+      pc.slice_merge = 1;
+      e = launch_pdl_coop(kern, dim3(p.num_ctas), dim3(C::kThreads), (size_t)lay.total, s, tk, tv, pc);
+      if (e == cudaSuccess) {
+        set_coop_launch_state(1);
+        return e;
+      }
+      (void)cudaGetLastError();
+      if (cs != cudaStreamCaptureStatusNone) return e;  // the capture is lost: report it
+      set_coop_launch_state(-1);
+    }
+  }
   return launch_pdl(kern, dim3(p.num_ctas), dim3(C::kThreads), (size_t)lay.total, s, tk, tv, p);
 }
 

@@ -62,6 +62,10 @@ struct DecodeParams {
   const int64_t* new_slots;
   float k_quant;
   float v_quant;
+  // 1: the grid is co-resident (cooperative launch), so every CTA that holds a
+  // part of a cut segment waits for the segment's last part and merges its own
+  // slice of the rows; 0: the CTA counting the last part merges all of them
+  int32_t slice_merge;
   // [B * Hkv] arrival counters of segments cut across CTAs, tagged with E
   // (any other contents read as zero): the last CTA to finish its part of a
   // segment merges the segment's partials
