@@ -59,6 +59,12 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle CPU-baseline sample length; <= 0 skips it")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="decode workloads: pool element type (e4m3: one scale per pool and tensor)")
+    ap.add_argument("--decode", default="plain", choices=["plain", "fused", "csr", "cascade"],
+                    help="decode workloads: the call a step makes (plain: append + decode; fused: "
+                         "paged_attention_decode_append; csr: append + the CSR call; cascade: append + "
+                         "cascade decode over the batch's shared prefix)")
     return ap.parse_args()
 
 
@@ -242,39 +248,112 @@ def rank_plan(name: str, rank: int):
     return base(1000 + 97 * rank)
 
 
-class DecodeRig:
-    """Device-resident decode workload: append + decode graph, and a decode-only graph."""
+def to_e4m3(pool, sc):
+    """Pool codes from torch's own e4m3 conversion (test inputs only; the timed
+    steps use the library's quantising append)."""
+    out8 = torch.empty(pool.shape, dtype=torch.float8_e4m3fn, device=pool.device)
+    step = max(1, (256 << 20) // max(1, pool[0].numel() * 4))
+    for i in range(0, pool.shape[0], step):
+        out8[i:i + step] = (pool[i:i + step].float() / sc).to(torch.float8_e4m3fn)
+    return out8
 
-    def __init__(self, plan, dev):
+
+class DecodeRig:
+    """Device-resident decode workload.  A step consumes the tensors of
+    ``inputs`` (q, this step's K/V rows and slots, the page table in the
+    mode's form) and runs the mode's calls: append + decode (plain, csr,
+    cascade) or the fused call."""
+
+    E4M3_SCALE = 0.02
+
+    def __init__(self, plan, dev, kv_dtype="bf16", mode="plain"):
         from serving_slot_mapping_gb300 import capi
         self.capi = capi
         self.plan = plan
+        self.mode = mode
         self.st = wl.materialize(plan, dev)
+        self.kv8 = kv_dtype == "e4m3"
+        self.ks = self.vs = self.E4M3_SCALE if self.kv8 else 1.0
+        if self.kv8 and mode == "cascade":
+            raise ValueError("cascade decode takes bf16 pools")
+        if self.kv8:
+            self.st.key_pool = to_e4m3(self.st.key_pool, self.ks)
+            self.st.value_pool = to_e4m3(self.st.value_pool, self.vs)
+            torch.cuda.empty_cache()
         self.out = torch.empty_like(self.st.q)
-        self.ws = capi.decode_workspace(plan.batch, plan.num_q_heads, self.st.key_pool)
-        self.msl = int(plan.seq_lens.max())
-
-    def append(self):
         st = self.st
-        self.capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping)
+        self.inputs = {"q": st.q, "key": st.key, "value": st.value, "slot_mapping": st.slot_mapping}
+        self.msl = int(plan.seq_lens.max())
+        if mode == "csr":
+            ip, ix, last = (torch.from_numpy(a).to(dev) for a in wl.csr_tables(plan))
+            self.inputs.update(kv_indptr=ip, kv_indices=ix, kv_last_page_len=last)
+        elif mode == "cascade":
+            pages = wl.shared_prefix_pages(plan)
+            if pages == 0:
+                raise ValueError(f"{plan.name}: no page shared by the whole batch")
+            pre, self.prefix_len, own_bt, own_lens = wl.cascade_tables(plan, pages, pages * plan.page_size)
+            self.inputs.update(prefix_pages=torch.from_numpy(pre).to(dev),
+                               block_table=torch.from_numpy(own_bt).to(dev),
+                               seq_lens=torch.from_numpy(own_lens).to(dev))
+            self.msl = int(own_lens.max())
+        else:
+            self.inputs.update(block_table=st.block_table, seq_lens=st.seq_lens)
+        self.ws = (capi.cascade_workspace(plan.batch, plan.num_q_heads, st.key_pool) if mode == "cascade"
+                   else capi.decode_workspace(plan.batch, plan.num_q_heads, st.key_pool))
+
+    def kv_bytes(self):
+        """Algorithmic K/V bytes a step's attention reads."""
+        return wl.decode_kv_bytes(self.plan) // (2 if self.kv8 else 1)
+
+    def append_with(self, t):
+        st = self.st
+        self.capi.paged_kv_append(st.key_pool, st.value_pool, t["key"], t["value"], t["slot_mapping"],
+                                  k_scale=self.ks, v_scale=self.vs)
+
+    def decode_with(self, t):
+        st, c, p = self.st, self.capi, self.plan
+        kw = dict(max_seq_len=self.msl, out=self.out, workspace=self.ws)
+        if self.mode == "csr":
+            c.paged_attention_decode_csr(st.key_pool, st.value_pool, t["q"], t["kv_indptr"], t["kv_indices"],
+                                         t["kv_last_page_len"], p.scale, k_scale=self.ks, v_scale=self.vs, **kw)
+        elif self.mode == "cascade":
+            c.paged_attention_decode_cascade(st.key_pool, st.value_pool, t["q"], t["prefix_pages"],
+                                             self.prefix_len, t["block_table"], t["seq_lens"], p.scale, **kw)
+        else:
+            c.paged_attention_decode(st.key_pool, st.value_pool, t["q"], t["block_table"], t["seq_lens"],
+                                     p.scale, k_scale=self.ks, v_scale=self.vs, **kw)
+
+    def step_with(self, t):
+        if self.mode == "fused":
+            st = self.st
+            self.capi.paged_attention_decode_append(
+                st.key_pool, st.value_pool, t["key"], t["value"], t["slot_mapping"], t["q"], t["block_table"],
+                t["seq_lens"], self.plan.scale, max_seq_len=self.msl, out=self.out, workspace=self.ws,
+                k_scale=self.ks, v_scale=self.vs)
+        else:
+            self.append_with(t)
+            self.decode_with(t)
+
+    def launches_per_step(self):
+        return {"fused": 1, "cascade": 4}.get(self.mode, 2)  # cascade: append, prefix pass, split, combine
+
+    # the device-resident forms
+    def append(self):
+        self.append_with(self.inputs)
 
     def decode(self):
-        st = self.st
-        self.capi.paged_attention_decode(st.key_pool, st.value_pool, st.q, st.block_table,
-                                         st.seq_lens, self.plan.scale, max_seq_len=self.msl,
-                                         out=self.out, workspace=self.ws)
+        self.decode_with(self.inputs)
 
     def step(self):
-        self.append()
-        self.decode()
+        self.step_with(self.inputs)
 
     def fused_step(self):
-        """The same step as one call (one launch): append + decode."""
+        """The plain step as one call (one launch): append + decode."""
         st = self.st
         self.capi.paged_attention_decode_append(st.key_pool, st.value_pool, st.key, st.value,
                                                 st.slot_mapping, st.q, st.block_table, st.seq_lens,
                                                 self.plan.scale, max_seq_len=self.msl, out=self.out,
-                                                workspace=self.ws)
+                                                workspace=self.ws, k_scale=self.ks, v_scale=self.vs)
 
 
 class PrefillRig:
@@ -304,25 +383,19 @@ class PrefillRig:
 
 def e2e_decode(rig: DecodeRig, steps, flush):
     """Same metric through the public API with host (pinned) inputs and output:
-    H2D of q, new K/V, slot_mapping, block_table, seq_lens; D2H of out."""
-    st = rig.st
-    names = ["q", "key", "value", "slot_mapping", "block_table", "seq_lens"]
-    host = {n: getattr(st, n).cpu().pin_memory() for n in names}
-    dev = {n: torch.empty_like(getattr(st, n)) for n in names}
+    H2D of the step's inputs (q, new K/V, slot_mapping, the page table in the
+    mode's form); D2H of out."""
+    host = {n: t.cpu().pin_memory() for n, t in rig.inputs.items()}
+    dev = {n: torch.empty_like(t) for n, t in rig.inputs.items()}
     out_h = torch.empty(rig.out.shape, dtype=rig.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
-    capi = rig.capi
     stream = torch.cuda.current_stream()
 
     def one():
-        for n in names:
+        for n in host:
             dev[n].copy_(host[n], non_blocking=True)
-        capi.paged_kv_append(st.key_pool, st.value_pool, dev["key"], dev["value"],
-                             dev["slot_mapping"])
-        capi.paged_attention_decode(st.key_pool, st.value_pool, dev["q"], dev["block_table"],
-                                    dev["seq_lens"], rig.plan.scale, max_seq_len=rig.msl,
-                                    out=rig.out, workspace=rig.ws)
+        rig.step_with(dev)
         out_h.copy_(rig.out, non_blocking=True)
 
     for _ in range(3):
@@ -421,9 +494,10 @@ def run_ours(args, rank, world, local):
     plan = rank_plan(args.workload, rank)
     if plan.kind == "prefill":
         return run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, bf16_sus, peak_src)
-    rig = DecodeRig(plan, dev)
+    rig = DecodeRig(plan, dev, args.kv_dtype, args.decode)
     g_step = capture(rig.step, stream)
-    g_dec = capture(rig.decode, stream)
+    # the attention call alone (fused: the step is that one call)
+    g_dec = capture(rig.step if args.decode == "fused" else rig.decode, stream)
     for _ in range(args.warmup):
         g_step.replay()
     torch.cuda.synchronize()
@@ -435,23 +509,30 @@ def run_ours(args, rank, world, local):
     times = timed_graph(g_step, args.steps, flush, stream)
     torch.cuda.synchronize()
     barrier(world)
-    # dominant kernel alone (the decode call: one launch, merges included), same flushing
+    # the attention call alone (plain: one launch, merges included), same flushing
     dec_times = timed_graph(g_dec, max(50, args.steps // 2), flush, stream)
     clocks = sampler.stop()
 
     ms_step = max_over_ranks(statistics.mean(times), world)
-    kv_bytes = wl.decode_kv_bytes(plan)
+    kv_bytes = rig.kv_bytes()
     total_kv = sum_over_ranks(float(kv_bytes), world)
     value = total_kv / (ms_step * 1e-3) / 1e9
     tokens_s = sum_over_ranks(float(plan.batch), world) / (ms_step * 1e-3)
 
     dec_ms = statistics.mean(dec_times)
-    dec_bytes = kv_bytes + wl.decode_io_bytes(plan)
+    # algorithmic bytes of the attention call: cascade reads the shared prefix once
+    unique = wl.decode_unique_kv_bytes(plan) if args.decode == "cascade" else None
+    dec_bytes = (unique if unique is not None else kv_bytes) + wl.decode_io_bytes(plan)
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = traffic_for(f"decode_split:{args.workload}")
+    variant = "" if (args.kv_dtype, args.decode) == ("bf16", "plain") else f":{args.kv_dtype}:{args.decode}"
+    traffic = traffic_for(f"decode_split:{args.workload}{variant}")
+    call = {"plain": "paged_attention_decode (decode_split_kernel, in-kernel merges)",
+            "fused": "paged_attention_decode_append (decode_split_kernel, fused append)",
+            "csr": "paged_attention_decode_csr (decode_split_kernel)",
+            "cascade": "paged_attention_decode_cascade (prefix pass + decode_split_kernel + combine)"}[args.decode]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "kernel": "paged_attention_decode (decode_split_kernel, in-kernel merges)",
+                "kernel": call + (" on e4m3 pools" if rig.kv8 else ""),
                 "algorithmic_bytes_per_launch": dec_bytes,
                 "ms_per_launch": round(dec_ms, 5), "peak_source": peak_src}
 
@@ -476,12 +557,17 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV, f16 products" if rig.kv8 else "bf16",
         "data": "synthetic",
         "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
                    "num_kv_heads": plan.num_kv_heads, "head_dim": plan.head_dim,
-                   "page_size": plan.page_size, "context": "U[512,4096]",
-                   "kv_bytes_per_step": kv_bytes, "step": "append 1 token/seq + decode",
+                   "page_size": plan.page_size,
+                   "context": f"{int(plan.seq_lens.min())}..{int(plan.seq_lens.max())} keys",
+                   "kv_dtype": args.kv_dtype, "decode_call": args.decode,
+                   "kv_bytes_per_step": kv_bytes,
+                   "unique_kv_bytes_per_step": wl.decode_unique_kv_bytes(plan) // (2 if rig.kv8 else 1),
+                   "step": "append 1 token/seq + decode" + (" (one call)" if args.decode == "fused" else ""),
                    "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_s, 1),
@@ -490,7 +576,7 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,  # per step: the append kernel and the decode kernel
+        "gpu_launches": rig.launches_per_step() * args.steps,
         "extra": extra,
     }
     return line
@@ -584,27 +670,8 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
     for name in ["gqa_decode", "long_gqa", "long_mqa"]:  # the same batches on e4m3 pools
         try:
             plan = wl.named_plan(name)
-            rig = DecodeRig(plan, dev)
-            ks, vs = 0.02, 0.02
-            # pool codes from torch's own e4m3 conversion (inputs only; the timed
-            # step is the library's quantising append + decode)
-            def to_e4m3(pool, sc):
-                out8 = torch.empty(pool.shape, dtype=torch.float8_e4m3fn, device=pool.device)
-                step = max(1, (256 << 20) // max(1, pool[0].numel() * 4))
-                for i in range(0, pool.shape[0], step):
-                    out8[i:i + step] = (pool[i:i + step].float() / sc).to(torch.float8_e4m3fn)
-                return out8
-            kp8 = to_e4m3(rig.st.key_pool, ks)
-            vp8 = to_e4m3(rig.st.value_pool, vs)
-            del rig.st.key_pool, rig.st.value_pool
-            torch.cuda.empty_cache()
-            msl = int(plan.seq_lens.max())
-            st = rig.st
-
-            def decode_fp8():
-                rig.capi.paged_attention_decode(kp8, vp8, st.q, st.block_table, st.seq_lens, plan.scale,
-                                                max_seq_len=msl, out=rig.out, workspace=rig.ws, k_scale=ks,
-                                                v_scale=vs)
+            rig = DecodeRig(plan, dev, "e4m3")
+            decode_fp8 = rig.decode
             g = capture(decode_fp8, stream)
             ms = statistics.mean(timed_graph(g, steps, flush, stream))
             kvb = wl.decode_kv_bytes(plan) // 2 + wl.decode_io_bytes(plan)
@@ -614,7 +681,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, steps=30):
                                   "speedup_vs_bf16_pool": None}
             if name in res and "decode_ms" in res[name]:
                 res[name + "_fp8"]["speedup_vs_bf16_pool"] = round(res[name]["decode_ms"] / ms, 3)
-            del rig, g, kp8, vp8
+            del rig, g
             torch.cuda.empty_cache()
         except Exception as ex:
             res[name + "_fp8"] = {"error": repr(ex)[:200]}
