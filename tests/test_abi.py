@@ -135,3 +135,22 @@ def test_e4m3_pool_validation(L):
     assert L.paged_attention_prefill(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4,
                                      FAKE, 64, 0.1, None) == capi.PA_ERR_UNSUPPORTED  # decode and append only
     assert _decode(L, _pool(dtype=3)) == capi.PA_ERR_DTYPE
+
+
+def test_decode_append_validation(L):
+    f = L.paged_attention_decode_append
+    p = _pool()
+
+    def call(pool=p, key=FAKE, value=FAKE, slots=FAKE, q=FAKE, out=ctypes.c_void_p(0x50000), batch=2, hq=32,
+             msl=64, scale=0.1, ws=None, wsb=0):
+        return f(ctypes.byref(pool), key, value, slots, q, out, batch, hq, FAKE, 4, FAKE, msl, scale, ws, wsb,
+                 None)
+    assert call(batch=0) == capi.PA_OK                                   # nothing to do
+    assert call(key=None) == capi.PA_ERR_NULL
+    assert call(slots=None) == capi.PA_ERR_NULL
+    assert call(slots=ctypes.c_void_p(0x40004)) == capi.PA_ERR_ALIGN     # int64 slots: 8 B
+    assert call(key=ctypes.c_void_p(0x40008)) == capi.PA_ERR_ALIGN       # 8 bf16 per access: 16 B
+    assert call(out=FAKE) == capi.PA_ERR_SHAPE                           # out aliases q
+    assert call(hq=12) == capi.PA_ERR_SHAPE
+    assert call(scale=float("nan")) == capi.PA_ERR_RANGE
+    assert call() == capi.PA_ERR_WORKSPACE                               # bf16 needs the decode workspace
