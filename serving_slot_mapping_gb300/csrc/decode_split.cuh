@@ -16,28 +16,36 @@
 //   page_size 8).  All units are laid out sequence-major and cut into
 //   `num_ctas` equal contiguous ranges, one persistent CTA per SM, so every
 //   CTA streams the same number of KV bytes whatever the context-length mix.
-// * A producer warp follows block_table and loads each stage (NBS blocks x HB
-//   heads of K and V) with TMA tensor copies through a 4-D view of the pool
-//   {64 dims, slots, kv_heads, slabs}: one box {64, 16, HB, D/64} lands as
-//   HB tiles of 16 rows x 128 B per slab with the 128-byte swizzle.  For 8
-//   KV heads a box is a 32 KB slice of one page; measured on GB300, one
-//   thread issuing 16 KB boxes streams ~7.7 TB/s while 2 KB boxes issued back
-//   to back reach only ~2.6 TB/s, so ops are kept few and large.
-//   A second producer warp bulk-copies, per segment, the query rows.
+// * Two producer warps (even and odd stages) follow block_table and load each
+//   stage (NBS blocks x HB heads of K and V) with TMA tensor copies through a
+//   4-D view of the pool {64 dims, slots, kv_heads, slabs}: one box
+//   {64, 16, HB, D/64} lands as HB tiles of 16 rows x 128 B per slab with the
+//   128-byte swizzle.  For 8 KV heads a box is a 32 KB slice of one page;
+//   measured on GB300, one thread issuing 16 KB boxes streams ~7.7 TB/s while
+//   2 KB boxes issued back to back reach only ~2.6 TB/s, so ops are kept few
+//   and large.  A third warp bulk-copies, per segment, the query rows.
 // * Eight consumer warps map to (head in box, block in stage, row tile of 16
 //   query heads): S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in,
 //   fp32 accumulate), online softmax in the log2 domain, output rescale
 //   skipped when no running max moved.  Each page is read from HBM once for
 //   all G query heads of its KV head (GQA/MQA reuse).  Every consumer waits
 //   on every stage in order, so no mbarrier parity wait can run a phase ahead.
+// * e4m3 pools (KV8): a box brings D code bytes per row (128- or 64-byte
+//   swizzle); ldmatrix reads the codes as 16-bit pairs and cvt turns them into
+//   the f16 B fragments of mma.sync m16n8k16 f16 (Q's dims and the output
+//   columns are permuted to match); k_scale is folded into the softmax scale,
+//   v_scale into the final normalisation.
 // * Keys at or past L_b are masked in S and their V rows are zeroed in shared
 //   memory, so stale or NaN-poisoned slots never reach the output.
 // * At a segment (sequence x head box) end, warps that shared a head merge in
 //   shared memory; a segment covering the whole sequence writes bf16 output,
 //   a segment cut by a range boundary leaves one fp32 partial (m, l, o) per
-//   CTA, and the CTA that finishes the segment's last part merges them, after
-//   its own range, with o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i
-//   (parts are counted in workspace words tagged with a per-launch epoch).
+//   CTA.  Parts are counted in workspace words tagged with a per-launch epoch;
+//   after its range every CTA holding a part waits until all are counted and
+//   merges a slice of the segment's rows (the grid is launched cooperatively,
+//   so all CTAs are resident; without that launch the CTA counting the last
+//   part merges the whole segment), with
+//   o = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
 //   Cascade decode instead leaves every segment's partials to the combine
 //   kernel in decode_bf16.cu.
 // * The kernel uses programmatic stream serialization: its prologue runs
