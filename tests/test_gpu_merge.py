@@ -141,3 +141,53 @@ def test_merge_e4m3_pools(cuda_device):
         exp = kv_fp8.paged_attention_decode_fp8(kc, vc, ks, vs, to_f64(bits(q)), plan.block_table,
                                                 plan.seq_lens, plan.scale)
         assert_close(out, exp, "bf16", f"e4m3 merge rep {rep}")
+
+
+_FALLBACK_SCRIPT = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[1] + "/tests")
+import oracle
+from serving_slot_mapping_gb300 import capi
+from serving_slot_mapping_gb300 import workloads as wl
+from _parity import assert_close, bits, to_f64
+dev = torch.device("cuda:0")
+plan = wl.gqa_decode_plan(batch=16, seed=6)
+st = wl.materialize(plan, dev)
+kp, vp = st.key_pool.clone(), st.value_pool.clone()
+capi.paged_kv_append(kp, vp, st.key, st.value, st.slot_mapping)  # eager: creates the device error word
+torch.cuda.synchronize()
+ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+out = torch.full_like(st.q, float("nan"))
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):  # the process's first decode launch: inside a capture
+    capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                max_seq_len=int(plan.seq_lens.max()), out=out, workspace=ws, stream=s)
+for rep in range(2):
+    st.q.copy_(torch.randn(st.q.shape, generator=torch.Generator().manual_seed(rep)).to(st.q.dtype))
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    exp = oracle.paged_attention_decode(to_f64(bits(kp)), to_f64(bits(vp)), to_f64(bits(st.q)),
+                                        plan.block_table, plan.seq_lens, plan.scale)
+    assert_close(out, exp, "bf16", f"whole-segment merge, replay {rep}")
+print("fallback merge ok")
+"""
+
+
+def test_merge_without_cooperative_launch():
+    """The merge used when the grid is not launched cooperatively (the CTA
+    counting a segment's last part merges all of it).  A process whose first
+    decode launch happens inside a stream capture never tries the cooperative
+    launch, so its graph replays take this path."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", _FALLBACK_SCRIPT, root], capture_output=True, text=True,
+                         timeout=600, cwd=root)
+    assert out.returncode == 0, (out.stdout[-1500:], out.stderr[-3000:])
+    assert "fallback merge ok" in out.stdout
