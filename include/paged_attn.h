@@ -133,10 +133,17 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  *               not shared by calls in flight at the same time.  Its
  *               contents need no initialisation: each call writes every
  *               partial it reads, and the per-segment arrival counters that
- *               pick the CTA merging a segment cut across CTAs carry the
- *               launch's grid id, so a word left by any earlier launch (or
- *               never written) counts as zero.  The merge runs inside the
- *               one decode kernel (no second launch).
+ *               schedule the merge of a segment cut across CTAs carry a tag
+ *               derived from a per-launch epoch kept at the workspace's start
+ *               (each launch reads it and stores the next), so a word left by
+ *               any earlier launch, a CUDA graph replay included, or never
+ *               written counts as zero.  The merge runs inside the one
+ *               decode kernel (no second launch).
+ * The decode kernel is a persistent grid of at most one CTA per SM, launched
+ * cooperatively (all CTAs resident at once: the CTAs that computed the parts
+ * of a cut segment each merge a slice of it), so its start can wait for SMs
+ * held by kernels on other streams.  Where the runtime refuses that launch,
+ * the CTA that counts a segment's last part merges the whole segment.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
  * query heads per KV head, q 16-byte aligned;
  * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of
