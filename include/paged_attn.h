@@ -145,7 +145,8 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  * held by kernels on other streams.  Where the runtime refuses that launch,
  * the CTA that counts a segment's last part merges the whole segment.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
- * query heads per KV head, q 16-byte aligned;
+ * query heads per KV head, q 16-byte aligned, at most 2^31 - 1 slots
+ * (num_pages * page_size) per pool (PA_ERR_RANGE beyond);
  * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of
  * the values the codes stand for (scale * k_scale * q . e4m3(K), outputs
  * times v_scale), computed with f16 products (every e4m3 value is an f16);

@@ -229,6 +229,9 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
                              int32_t num_q_heads, const Table& t, int32_t max_seq_len, float scale, void* workspace,
                              size_t workspace_bytes, pa::DecodeParams* p, int reserved_sms = 0) {
   const int32_t group = num_q_heads / pool->num_kv_heads;
+  // the decode kernel's TMA boxes address a pool row (slot) with a 32-bit
+  // coordinate: at most 2^31 - 1 slots per pool
+  if (pool->num_pages * (int64_t)pool->page_size > INT32_MAX) return PA_ERR_RANGE;
   if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
   const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
   const int sms = num_sms() - reserved_sms;
