@@ -146,7 +146,8 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  * the CTA that counts a segment's last part merges the whole segment.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
  * query heads per KV head, q 16-byte aligned, at most 2^31 - 1 slots
- * (num_pages * page_size) per pool (PA_ERR_RANGE beyond);
+ * (num_pages * page_size) per pool and batch * ceil(max_seq_len / 16) below
+ * 2^31 (PA_ERR_RANGE beyond);
  * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of
  * the values the codes stand for (scale * k_scale * q . e4m3(K), outputs
  * times v_scale), computed with f16 products (every e4m3 value is an f16);

@@ -232,6 +232,9 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   // the decode kernel's TMA boxes address a pool row (slot) with a 32-bit
   // coordinate: at most 2^31 - 1 slots per pool
   if (pool->num_pages * (int64_t)pool->page_size > INT32_MAX) return PA_ERR_RANGE;
+  // ... and counts the batch's 16-key blocks (shared pages counted per
+  // sequence) in 32 bits
+  if ((int64_t)batch * (((int64_t)max_seq_len + 15) / 16) > INT32_MAX) return PA_ERR_RANGE;
   if (!aligned(q, 16) || !aligned(out, 4)) return PA_ERR_ALIGN;
   const int hb = pa::decode_heads_per_box(pool->num_kv_heads, group, pool->page_size);
   const int sms = num_sms() - reserved_sms;

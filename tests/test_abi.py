@@ -87,6 +87,7 @@ def test_decode_validation(L):
     assert _decode(L, _pool(k=0x10008)) == capi.PA_ERR_ALIGN         # bf16 pool needs 16 B
     assert _decode(L, _pool(), ws=None, wsb=0) == capi.PA_ERR_WORKSPACE
     assert _decode(L, _pool(P=1 << 27)) == capi.PA_ERR_RANGE         # 2^31 slots: past the 32-bit row
+    assert _decode(L, _pool(), batch=40000, mb=1 << 20, msl=1 << 24) == capi.PA_ERR_RANGE  # 2^30+ blocks
 
 
 def test_prefill_validation(L):
