@@ -398,6 +398,8 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
     return pa::launch_attn_f32(p, num_sms(), s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
   if (batch > 65535 || pool->num_kv_heads > 65535) return PA_ERR_RANGE;  // grid y/z limits
+  // a sequence's packed rows (token x G heads of one KV head) are 32-bit in the kernel
+  if ((int64_t)max_q_len * group > INT32_MAX / 2) return PA_ERR_RANGE;
   pa::PrefillParams p{};
   p.pool = g;
   p.q = q;

@@ -101,6 +101,8 @@ def test_prefill_validation(L):
              0.1, None) == capi.PA_OK                             # nothing to do
     assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4, FAKE, 64,
              float("inf"), None) == capi.PA_ERR_RANGE
+    assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 1 << 29, FAKE, 4, FAKE, 64,
+             0.1, None) == capi.PA_ERR_RANGE                      # 2^29 tokens x G 4 packed rows
     p4 = _pool(ps=4)                                                # bf16: page_size >= 8
     assert f(ctypes.byref(p4), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4, FAKE, 16,
              0.1, None) == capi.PA_ERR_UNSUPPORTED
