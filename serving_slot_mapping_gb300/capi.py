@@ -145,6 +145,22 @@ def make_pool(key_pool: torch.Tensor, value_pool: torch.Tensor, k_scale: float =
                     _dtype_code(key_pool.dtype), float(k_scale), float(v_scale))
 
 
+def _q_out(q, out, key_pool):
+    """Check ``q [rows, Hq, D]`` against the pool (bf16 for bf16 and e4m3
+    pools, f32 for f32 pools) and return ``out`` of the same shape and dtype
+    (allocated when None)."""
+    want = torch.bfloat16 if key_pool.dtype in (torch.bfloat16, torch.float8_e4m3fn) else key_pool.dtype
+    _contig(q, "q")
+    if q.dim() != 3 or q.dtype != want or q.shape[2] != key_pool.shape[3]:
+        raise ValueError(f"q must be [rows, num_q_heads, {key_pool.shape[3]}] of {want}")
+    if out is None:
+        return torch.empty_like(q)
+    _contig(out, "out")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q in shape and dtype")
+    return out
+
+
 def paged_kv_append(key_pool, value_pool, key, value, slot_mapping, stream=None, k_scale=1.0,
                     v_scale=1.0):
     """Scatter ``key/value [T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 [T]).
@@ -196,8 +212,7 @@ def paged_attention_decode(key_pool, value_pool, q, block_table, seq_lens, scale
     mb = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = mb * pool.page_size
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     if workspace is None:
         workspace = decode_workspace(B, hq, key_pool)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -225,13 +240,16 @@ def paged_attention_decode_append(key_pool, value_pool, key, value, slot_mapping
         raise TypeError("block_table and seq_lens must be int32")
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
-    if key.shape[0] != B or value.shape[0] != B or slot_mapping.numel() != B:
-        raise ValueError("one new token per sequence: key/value [B, Hkv, D], slot_mapping [B]")
+    row_dtype = torch.bfloat16 if key_pool.dtype == torch.float8_e4m3fn else key_pool.dtype
+    for n, t in (("key", key), ("value", value)):
+        if t.dtype != row_dtype or t.numel() != B * pool.num_kv_heads * pool.head_dim:
+            raise ValueError(f"{n} must be [B, num_kv_heads, head_dim] of {row_dtype}")
+    if slot_mapping.numel() != B:
+        raise ValueError("one new token per sequence: slot_mapping [B]")
     mb = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = mb * pool.page_size
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     if workspace is None:
         workspace = decode_workspace(B, hq, key_pool)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -261,8 +279,7 @@ def paged_attention_decode_static_scratch(key_pool, value_pool, q, block_table, 
     mb = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = mb * pool.page_size
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     st = lib().paged_attention_decode_static_scratch(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
                                                      _ptr(block_table), mb, _ptr(seq_lens),
                                                      int(max_seq_len), float(scale),
@@ -300,8 +317,7 @@ def paged_attention_decode_cascade(key_pool, value_pool, q, prefix_block_ids, pr
     mb = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = mb * pool.page_size
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     if workspace is None:
         workspace = cascade_workspace(B, hq, key_pool)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -330,8 +346,7 @@ def paged_attention_prefill(key_pool, value_pool, q, query_start_loc, block_tabl
     mb = block_table.shape[1]
     if max_seq_len is None:
         max_seq_len = mb * pool.page_size
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     st = lib().paged_attention_prefill(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
                                        _ptr(query_start_loc), T, int(max_q_len),
                                        _ptr(block_table), mb, _ptr(seq_lens), int(max_seq_len),
@@ -366,8 +381,7 @@ def paged_attention_decode_csr(key_pool, value_pool, q, kv_indptr, kv_indices, k
     _contig(q, "q")
     B, hq, d = q.shape
     ip, ix, nix, last = _csr_args(kv_indptr, kv_indices, kv_last_page_len)
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     if workspace is None:
         workspace = decode_workspace(B, hq, key_pool)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -387,8 +401,7 @@ def paged_attention_prefill_csr(key_pool, value_pool, q, query_start_loc, kv_ind
     T, hq, d = q.shape
     B = query_start_loc.numel() - 1
     ip, ix, nix, last = _csr_args(kv_indptr, kv_indices, kv_last_page_len)
-    if out is None:
-        out = torch.empty_like(q)
+    out = _q_out(q, out, key_pool)
     st = lib().paged_attention_prefill_csr(ctypes.byref(pool), _ptr(q), _ptr(out), B, hq,
                                            _ptr(query_start_loc), T, int(max_q_len), ip, ix, nix, last,
                                            int(max_seq_len), float(scale), _stream(stream))
