@@ -125,6 +125,23 @@ def file_hash(*paths):
     return h.hexdigest()[:16]
 
 
+def repeatability(times, repeats=5, limit=1.05):
+    """The timed steps cut into ``repeats`` consecutive runs: the median of the
+    runs' mean step times, their spread (slowest / fastest run) and whether the
+    spread is within ``limit`` (a number whose runs disagree by more is flagged
+    as not reportable)."""
+    times = [float(t) for t in times]
+    k = max(1, min(repeats, len(times)))
+    if not times:
+        return {"repeats": 0, "median_ms": None, "spread": None, "reportable": False}
+    size = len(times) // k
+    runs = [statistics.mean(times[i * size:(i + 1) * size if i < k - 1 else len(times)]) for i in range(k)]
+    spread = max(runs) / min(runs) if min(runs) > 0 else None
+    return {"repeats": k, "median_ms": round(statistics.median(runs), 5),
+            "spread": round(spread, 4) if spread is not None else None,
+            "reportable": spread is not None and spread <= limit}
+
+
 def traffic_for(kernel_key: str):
     """Per-launch DRAM bytes from a committed ncu capture, if the kernel source
     is unchanged since the capture (else None)."""
@@ -572,6 +589,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_hbm_peak": round(100.0 * value / (hbm * world), 2),
+        "repeatability": repeatability(times),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -621,6 +639,7 @@ def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, b
                      "kernel": "paged_attention_prefill", "ms_per_launch": round(pf_ms, 5),
                      "peak_source": peak_src, "peak_sustained": bf16_sus},
         "clocks": clocks, "gpu_launches": 2 * args.steps,
+        "repeatability": repeatability(times),
     }
 
 
