@@ -24,7 +24,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .paged_attention import paged_attention_decode
+from .paged_attention import paged_attention_decode, paged_attention_prefill
 
 E4M3_MAX = 448.0
 
@@ -115,6 +115,15 @@ def paged_attention_decode_fp8(key_codes, value_codes, k_scale, v_scale, q, bloc
     """Decode over e4m3 pools: the plain decode on the values the codes stand for."""
     return paged_attention_decode(dequantize(key_codes, k_scale), dequantize(value_codes, v_scale), q,
                                   block_table, seq_lens, scale, seqs=seqs)
+
+
+def paged_attention_prefill_fp8(key_codes, value_codes, k_scale, v_scale, q, query_start_loc, block_table,
+                                seq_lens, scale, rows=None):
+    """Varlen causal prefill over e4m3 pools: the plain prefill (token i of
+    sequence b at position L_b - n_b + i sees keys 0..that position) on the
+    values the codes stand for (reading 4)."""
+    return paged_attention_prefill(dequantize(key_codes, k_scale), dequantize(value_codes, v_scale), q,
+                                   query_start_loc, block_table, seq_lens, scale, rows=rows)
 
 
 def paged_attention_decode_append_fp8(key_codes, value_codes, key, value, slot_mapping, k_scale, v_scale,
