@@ -86,3 +86,27 @@ def test_reference_arm_two_ranks_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_first_sequences_is_a_compact_prefix_of_the_batch():
+    bench = _load_bench()
+    full = bench.rank_plan("long_gqa", 0)
+    small = bench.rank_plan("long_gqa", 0, batch=16)
+    assert small.batch == 16 and (small.seq_lens == full.seq_lens[:16]).all()
+    assert (small.num_q_heads, small.num_kv_heads, small.head_dim) == (32, 8, 128)
+    used = sum((int(L) + 15) // 16 for L in small.seq_lens)
+    assert small.num_pages == used + -(-used // 10)       # its own pool: used pages + 10 % free
+    assert bench.rank_plan("gqa_decode", 0, batch=0).batch == 32
+    with pytest.raises(ValueError):
+        bench.rank_plan("shared_prefix", 0, batch=8)      # shared pages cannot be cut
+
+
+def test_cpu_baseline_legs_report_all_cores_and_one_thread():
+    """The oracle CPU baseline runs in subprocesses with the BLAS thread count
+    fixed through the environment: every core, then one thread."""
+    bench = _load_bench()
+    cpu = bench.cpu_baseline("gqa_decode", 2, 0.05, "decode")
+    assert cpu["kind"] == "oracle" and cpu["unit"] == "GB/s" and cpu["value"] > 0
+    assert cpu["cores"] == bench.cpu_cores() and cpu["one_thread"]["cores"] == 1
+    assert cpu["one_thread"]["value"] > 0 and cpu["full_step_s_extrapolated"] > 0
+    assert "first 2/2 sequences" in cpu["sample"]
