@@ -64,7 +64,7 @@ typedef enum pa_dtype {
   PA_DTYPE_F32 = 0,        /* float32 pool, q and out                           */
   PA_DTYPE_BF16 = 1,       /* bfloat16 pool, q and out; fp32 accumulation       */
   PA_DTYPE_FP8_E4M3 = 2    /* e4m3 pool with k_scale / v_scale; bf16 q, out and
-                              appended rows (decode and append only)            */
+                              appended rows                                     */
 } pa_dtype;
 
 /* One layer's KV page pool (mobius PR #395 "ONNX I/O contract":
@@ -295,6 +295,9 @@ pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key,
  * - All calls share the one array, which keeps the last call's contents;
  *   calls whose kernels overlap on the GPU (different streams, or unordered
  *   host threads) race on it.  No part of it needs to start zeroed.
+ * - The stream must belong to the current device (the array's address is
+ *   that device's); a stream of another device gives PA_ERR_CUDA and nothing
+ *   is launched.
  * - bf16 and e4m3 pools only (PA_ERR_UNSUPPORTED for f32, whose decode needs no
  *   workspace anyway).  A call whose partials would not fit, i.e. when
  *   paged_attention_decode_workspace_size(...) exceeds
@@ -329,7 +332,12 @@ pa_status paged_attention_decode_static_scratch(const pa_kv_pool* pool, const vo
  * max_q_len        host upper bound of n_b (sizes the launch).
  * block_table, seq_lens, max_seq_len, scale: as for decode.
  * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most
- * 32 query heads per KV head; e4m3 pools: PA_ERR_UNSUPPORTED;
+ * 32 query heads per KV head;
+ * e4m3 pools: the bf16 limits, q 16-byte aligned; q and out are bf16; the
+ * attention is that of the values the codes stand for (scale * k_scale *
+ * q . e4m3(K), outputs times v_scale), computed with f16 products: q is
+ * rounded to f16 (exact for bf16 values of magnitude 2^-14 .. 65504), the
+ * codes are exact in f16, and the softmax weights are rounded to f16;
  * f32 path: head_dim <= 256, any page_size.
  */
 pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out,
@@ -348,6 +356,29 @@ pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* o
  * up; *detail holds the offending value.  Either pointer may be NULL.
  */
 pa_status paged_device_error(int64_t* code, int64_t* detail);
+
+/*
+ * pa_testing_decode_part_wait -- TEST HOOK, not for production use: the pages
+ * have no counterpart.  paged_attention_decode (bf16 and e4m3 pools, same
+ * arguments, same workspace) with the one wait inside the decode kernel that
+ * depends on other CTAs -- a CTA holding part of a sequence's keys waits for
+ * the other CTAs' parts before merging its slice of the rows -- given the
+ * limit `wait_ns` (1 us .. 2 s; every public call uses 2 s) and
+ * `extra_parts` (0 .. 1024) parts added to the count each such wait expects.
+ * With extra_parts > 0 those parts never arrive, so every such wait runs out
+ * after wait_ns: the kernel records code 5 (a bounded wait gave up) in the
+ * device error word, finishes without those parts and returns; the outputs
+ * of the affected sequences are then unspecified.  It exists so that the
+ * failure path of the bounded wait can be exercised without a fault or a
+ * hang; a later call on the same workspace is unaffected.  PA_ERR_RANGE for
+ * a limit or count outside the ranges above.
+ */
+pa_status pa_testing_decode_part_wait(const pa_kv_pool* pool, const void* q, void* out,
+                                      int32_t batch, int32_t num_q_heads,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                      void* workspace, size_t workspace_bytes, uint64_t wait_ns,
+                                      int32_t extra_parts, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* pa_status_string(int32_t status);

@@ -65,6 +65,9 @@ SIGNATURES = {
                                            _c_void_p]),
     "paged_attention_prefill": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i64,
                                        _i32, _c_void_p, _i32, _c_void_p, _i32, _f32, _c_void_p]),
+    "pa_testing_decode_part_wait": (_i32, [_PPOOL, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _i32,
+                                           _c_void_p, _i32, _f32, _c_void_p, _sz, ctypes.c_uint64, _i32,
+                                           _c_void_p]),
     "paged_device_error": (_i32, [ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_abi_version": (_i32, []),
@@ -330,12 +333,14 @@ def paged_attention_decode_cascade(key_pool, value_pool, q, prefix_block_ids, pr
 
 
 def paged_attention_prefill(key_pool, value_pool, q, query_start_loc, block_table, seq_lens,
-                            scale, max_q_len, max_seq_len=None, out=None, stream=None):
+                            scale, max_q_len, max_seq_len=None, out=None, stream=None, k_scale=1.0,
+                            v_scale=1.0):
     """Varlen causal prefill: ``q [T, Hq, D]`` packed by ``query_start_loc`` int32 [B+1].
 
     ``max_q_len`` is a host upper bound of the per-sequence new-token counts.
+    ``k_scale`` / ``v_scale`` apply to e4m3 pools.
     """
-    pool = make_pool(key_pool, value_pool)
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
     _contig(q, "q")
     _contig(block_table, "block_table")
     T, hq, d = q.shape
@@ -393,9 +398,11 @@ def paged_attention_decode_csr(key_pool, value_pool, q, kv_indptr, kv_indices, k
 
 
 def paged_attention_prefill_csr(key_pool, value_pool, q, query_start_loc, kv_indptr, kv_indices,
-                                kv_last_page_len, scale, max_q_len, max_seq_len, out=None, stream=None):
-    """Varlen causal prefill with the page table in CSR form."""
-    pool = make_pool(key_pool, value_pool)
+                                kv_last_page_len, scale, max_q_len, max_seq_len, out=None, stream=None,
+                                k_scale=1.0, v_scale=1.0):
+    """Varlen causal prefill with the page table in CSR form (``k_scale`` /
+    ``v_scale`` for e4m3 pools)."""
+    pool = make_pool(key_pool, value_pool, k_scale, v_scale)
     _contig(q, "q")
     _contig(query_start_loc, "query_start_loc")
     T, hq, d = q.shape

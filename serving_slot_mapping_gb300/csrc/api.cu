@@ -278,9 +278,9 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
 
 // Cascade decode, prefix pass: key chunks per (row tile, KV head), an upper
 // bound on the chunk count.  The prefix pass runs beside the split kernel
-// (which leaves it the SMs it needs), so it takes about an eighth of the SMs;
-// fewer chunks also mean fewer fp32 partials (B*Hq*D*4 bytes each) for the
-// combine kernel to read back.
+// (which leaves it the SMs it needs), so it takes about a quarter of the SMs
+// (num_SMs / 4 CTAs in all); fewer chunks also mean fewer fp32 partials
+// (B*Hq*D*4 bytes each) for the combine kernel to read back.
 int cascade_chunk_target(int32_t batch, int32_t group, int32_t num_kv_heads) {
   const int64_t row_ctas = ((int64_t)batch * group + 255) / 256;
   const int64_t t = num_sms() / (4 * row_ctas * num_kv_heads);
@@ -364,7 +364,6 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
                        int32_t max_seq_len, float scale, void* stream) {
   pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
   if (st != PA_OK) return st;
-  if (kv8(pool)) return PA_ERR_UNSUPPORTED;  // e4m3 pools: decode and append only
   if (total_q < 0 || max_q_len < 0 || total_q > INT32_MAX) return PA_ERR_SHAPE;
   if (batch == 0 || total_q == 0) return PA_OK;
   if (max_q_len == 0) return PA_ERR_SHAPE;
@@ -374,6 +373,7 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
   if (q == out) return PA_ERR_SHAPE;
   if (!aligned(query_start_loc, 4)) return PA_ERR_ALIGN;
   if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  if (kv8(pool) && !aligned(q, 16)) return PA_ERR_ALIGN;  // e4m3 pools: q rows read 16 bytes at a time
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const pa::PoolGeom g = geom(pool);
   const int32_t group = num_q_heads / pool->num_kv_heads;
@@ -416,7 +416,10 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
   p.group = group;
   p.max_blocks = t.max_blocks;
   p.max_q_len = max_q_len;
-  p.scale_log2 = (float)((double)scale * kLog2e);
+  // e4m3 pools: S = scale * k_scale * q . e4m3(K), O = v_scale * softmax(S) e4m3(V)
+  p.kv8 = kv8(pool) ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * (kv8(pool) ? (double)pool->k_scale : 1.0) * kLog2e);
+  p.v_scale = kv8(pool) ? pool->v_scale : 1.f;
   p.err = error_word();
   return pa::launch_prefill_bf16(p, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -446,6 +449,32 @@ pa_status paged_attention_decode(const pa_kv_pool* pool, const void* q, void* ou
                                  size_t workspace_bytes, void* stream) {
   return decode_impl(pool, q, out, batch, num_q_heads, dense_table(block_table, max_blocks_per_seq, seq_lens),
                      max_seq_len, scale, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_testing_decode_part_wait(const pa_kv_pool* pool, const void* q, void* out, int32_t batch,
+                                      int32_t num_q_heads, const int32_t* block_table,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                                      float scale, void* workspace, size_t workspace_bytes, uint64_t wait_ns,
+                                      int32_t extra_parts, void* stream) {
+  if (pool == nullptr) return PA_ERR_NULL;
+  if (pool->dtype != PA_DTYPE_BF16 && pool->dtype != PA_DTYPE_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  // a short limit (1 us .. 2 s) and a bounded count: the hook can only
+  // shorten a wait, never lengthen one
+  if (wait_ns < 1000u || wait_ns > 2000000000u || extra_parts < 0 || extra_parts > 1024) return PA_ERR_RANGE;
+  const Table t = dense_table(block_table, max_blocks_per_seq, seq_lens);
+  pa_status st = check_attention(pool, batch, num_q_heads, t.max_blocks, max_seq_len, scale);
+  if (st != PA_OK) return st;
+  if (batch == 0) return PA_OK;
+  if (q == nullptr || out == nullptr) return PA_ERR_NULL;
+  st = check_table(t);
+  if (st != PA_OK) return st;
+  if (q == out) return PA_ERR_SHAPE;
+  pa::DecodeParams p;
+  st = bf16_decode_params(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, &p);
+  if (st != PA_OK) return st;
+  p.part_wait_ns = wait_ns;
+  p.test_extra_parts = extra_parts;
+  return pa::launch_decode_bf16(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key, const void* value,
@@ -559,6 +588,7 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
   pp.batch_rows = batch;
   pp.prefix_len = prefix_len;
   pp.chunk_tiles = chunk_tiles;
+  pp.v_scale = 1.f;
   p.pre_o = pre_o;
   p.pre_ml = pre_ml;
   p.pre_chunks = chunks;

@@ -189,8 +189,8 @@ cudaError_t launch_split_only(const DecodeParams& p, cudaStream_t s) {
   const int64_t rows = p.pool.num_pages * (int64_t)p.pool.page_size;
   CUtensorMap tk, tv;
   if (p.kv8) {
-    if (!encode_pool_tmap_u8(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box) ||
-        !encode_pool_tmap_u8(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box))
+    if (!encode_pool_tmap_u8(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, true) ||
+        !encode_pool_tmap_u8(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, R, p.heads_per_box, true))
       return cudaErrorInvalidValue;
     if (p.new_k != nullptr) return launch_split_fused(p, tk, tv, RT, s);
     return D == 128 ? launch_split_d<128, true, false>(p, tk, tv, RT, s)

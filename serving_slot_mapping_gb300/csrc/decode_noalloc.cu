@@ -17,7 +17,13 @@
 // kernels overlap on the GPU (on different streams, or on one device from
 // several host threads without ordering) race on it.  Nothing in it needs to
 // start zeroed: every partial a call reads is written earlier in the same
-// launch, and the arrival counters carry the launch's grid id.
+// launch, and the arrival counters carry a tag derived from a per-launch
+// epoch word kept at the array's start (each launch reads it and stores the
+// next), so counts left by an earlier call read as zero.
+//
+// The stream must belong to the current device: the array's address is the
+// current device's, so a call whose stream is on another GPU is refused
+// (PA_ERR_CUDA) before anything is launched.
 #include <atomic>
 
 #include "../../include/paged_attn.h"
@@ -54,6 +60,11 @@ extern "C" pa_status paged_attention_decode_static_scratch(
   const size_t need = paged_attention_decode_workspace_size(batch, num_q_heads, pool->num_kv_heads,
                                                             pool->head_dim, pool->dtype);
   if (need > (size_t)PA_DECODE_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+  // the scratch address below is the current device's: the kernel must run there
+  int cur = -1, sdev = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess ||
+      cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess || sdev != cur)
+    return PA_ERR_CUDA;
   void* scratch = nullptr;
   const pa_status st = scratch_address(&scratch);
   if (st != PA_OK) return st;

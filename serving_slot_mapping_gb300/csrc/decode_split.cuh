@@ -288,7 +288,7 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   using C = Cfg<D, HB, RT, KV8>;
   Layout L;
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
-  const int merge = C::NBS > 1 ? C::NBS * HB * G * (D + 2) * 4 : 0;
+  const int merge = C::NBS > 1 ? HB * G * (D + 2) * 4 : 0;  // one slot: the chained merge below
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
   const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 128 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto qfull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
   auto qempty_bar = [&](int s) { return bars + 8u * (2 * S + 2 + s); };
-  float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [NBS][HB][G][D]
-  float* mrg_ml = mrg_o + NBS * HB * G * D;                           // [NBS][HB][G][2]
+  float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [HB][G][D]
+  float* mrg_ml = mrg_o + HB * G * D;                                 // [HB][G][2]
   int* prefix = reinterpret_cast<int*>(smem + lay.prefix_off);        // [B+1] 16-key blocks before b
   // segments this CTA merges (some of) after its range: [0] = count, then
   // kPend ints each (b, head box, c0, span, parts, this CTA's part index);
@@ -862,8 +862,76 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     const int64_t seg_id = (int64_t)cc.b * Hg + cc.hk;
     const int64_t pslot = (seg_id + c) * HB + h;  // unique per (segment, CTA, head)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)hk * G) * D;
-    if (NBS == 1) {
-      // this warp holds its rows' whole segment state: write directly
+    if (NBS > 1) {
+      // NBS warps share each head and row tile, each with the state of its
+      // block of every stage: chained through one shared-memory slot, warp
+      // NBS - 1 hands its state to warp NBS - 2, ... down to warp 0 (one slot
+      // instead of NBS leaves room for another stage of the ring).
+      // o_w = 2^(m_w - M) o_w + 2^(m_x - M) o_x, the same for l, M = max(m_w, m_x).
+      float* mo = mrg_o + (h * G) * D;
+      float* mml = mrg_ml + (h * G) * 2;
+      auto set_pair = [&](int x, int half, float2 v) {
+        const int k = x >> 1, pi = x & 1;
+        if (KV8) {
+          o[2 * k][2 * half + pi] = v.x;
+          o[2 * k + 1][2 * half + pi] = v.y;
+        } else {
+          o[2 * k + pi][2 * half] = v.x;
+          o[2 * k + pi][2 * half + 1] = v.y;
+        }
+      };
+#pragma unroll 1
+      for (int w = NBS - 1; w >= 1; --w) {
+        if (jw == w) {
+          if ((lane & 3) == 0) {
+            if (rA < G) { mml[rA * 2] = m0; mml[rA * 2 + 1] = la; }
+            if (rB < G) { mml[rB * 2] = m1; mml[rB * 2 + 1] = lb; }
+          }
+#pragma unroll
+          for (int x = 0; x < D / 8; ++x) {
+            const int col = out_col(x);
+            if (rA < G) *reinterpret_cast<float2*>(&mo[rA * D + col]) = out_pair(o, x, 0);
+            if (rB < G) *reinterpret_cast<float2*>(&mo[rB * D + col]) = out_pair(o, x, 1);
+          }
+        }
+        named_barrier(1, C::kConsumers * 32);
+        if (jw == w - 1) {
+          float fa = 1.f, ga = 0.f, fb = 1.f, gb = 0.f;  // weights of mine / the handed-over state
+          if (rA < G) {
+            const float mx = mml[rA * 2], M = fmaxf(m0, mx);
+            fa = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+            ga = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
+            la = la * fa + mml[rA * 2 + 1] * ga;
+            m0 = M;
+          }
+          if (rB < G) {
+            const float mx = mml[rB * 2], M = fmaxf(m1, mx);
+            fb = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+            gb = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
+            lb = lb * fb + mml[rB * 2 + 1] * gb;
+            m1 = M;
+          }
+#pragma unroll
+          for (int x = 0; x < D / 8; ++x) {
+            const int col = out_col(x);
+            float2 va = out_pair(o, x, 0), vb = out_pair(o, x, 1);
+            if (rA < G) {
+              const float2 t = *reinterpret_cast<const float2*>(&mo[rA * D + col]);
+              va = make_float2(va.x * fa + t.x * ga, va.y * fa + t.y * ga);
+            }
+            if (rB < G) {
+              const float2 t = *reinterpret_cast<const float2*>(&mo[rB * D + col]);
+              vb = make_float2(vb.x * fb + t.x * gb, vb.y * fb + t.y * gb);
+            }
+            set_pair(x, 0, va);
+            set_pair(x, 1, vb);
+          }
+        }
+        named_barrier(1, C::kConsumers * 32);
+      }
+    }
+    if (jw == 0) {
+      // this warp holds its rows' whole segment state: write it
       // v_scale: e4m3 V codes stand for code * v_scale (1 for bf16 pools)
       const float ia = la > 0.f ? p.v_scale / la : 0.f, ib = lb > 0.f ? p.v_scale / lb : 0.f;
 #pragma unroll
@@ -882,46 +950,6 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         if (rA < G) p.part_ml[pslot * G + rA] = make_float2(m0, la);
         if (rB < G) p.part_ml[pslot * G + rB] = make_float2(m1, lb);
       }
-    } else {
-      // NBS warps share each head: merge through shared memory
-      float* mo = mrg_o + ((jw * HB + h) * G) * D;
-      float* mml = mrg_ml + ((jw * HB + h) * G) * 2;
-      if ((lane & 3) == 0) {
-        if (rA < G) { mml[rA * 2] = m0; mml[rA * 2 + 1] = la; }
-        if (rB < G) { mml[rB * 2] = m1; mml[rB * 2 + 1] = lb; }
-      }
-#pragma unroll
-      for (int x = 0; x < D / 8; ++x) {
-        const int col = out_col(x);
-        if (rA < G) *reinterpret_cast<float2*>(&mo[rA * D + col]) = out_pair(o, x, 0);
-        if (rB < G) *reinterpret_cast<float2*>(&mo[rB * D + col]) = out_pair(o, x, 1);
-      }
-      named_barrier(1, C::kConsumers * 32);
-      for (int idx = tid; idx < HB * G * D; idx += C::kConsumers * 32) {
-        const int hh = idx / (G * D);
-        const int g = (idx / D) % G, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NBS; ++w) M = fmaxf(M, mrg_ml[((w * HB + hh) * G + g) * 2]);
-        float acc = 0.f, den = 0.f;
-#pragma unroll
-        for (int w = 0; w < NBS; ++w) {
-          const float mw = mrg_ml[((w * HB + hh) * G + g) * 2];
-          const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-          acc += f * mrg_o[((w * HB + hh) * G + g) * D + d];
-          den += f * mrg_ml[((w * HB + hh) * G + g) * 2 + 1];
-        }
-        const int64_t hkk = (int64_t)cc.hk * HB + hh;
-        if (complete) {
-          static_cast<__nv_bfloat16*>(p.out)[((int64_t)cc.b * Hq + hkk * G + g) * D + d] =
-              __float2bfloat16_rn(den > 0.f ? acc * p.v_scale / den : 0.f);
-        } else {
-          const int64_t ps_ = (seg_id + c) * HB + hh;
-          p.part_o[(ps_ * G + g) * D + d] = acc;
-          if (d == 0) p.part_ml[ps_ * G + g] = make_float2(M, den);
-        }
-      }
-      named_barrier(1, C::kConsumers * 32);
     }
     if (!complete && p.pre_chunks == 0) {
       // This CTA's part of a segment cut across CTAs is written.  Publish and
@@ -952,7 +980,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
           ent[1] = cc.hk;
           ent[2] = c0;
           ent[3] = c1 - c0 + 1;  // the merge walks the CTA span (empty CTAs weigh 0)
-          ent[4] = p.slice_merge ? arrivals : 1;
+          ent[4] = p.slice_merge ? arrivals + p.test_extra_parts : 1;
           ent[5] = p.slice_merge ? mine : 0;
           pending[0] = e + 1;
         }
@@ -973,11 +1001,12 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         if (tid == 0) {
           const unsigned long long tag = *tag_slot;
           const unsigned long long* cnt = p.seg_count + (int64_t)b * Hg + hkb;
+          const unsigned long long limit = p.part_wait_ns != 0 ? p.part_wait_ns : kWaitLimitNs;
           const unsigned long long t0 = global_ns();
           for (;;) {
             const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(cnt);
             if ((w >> 16) == tag && (int)(w & 0xFFFFu) >= parts) break;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit) {
               record_error(p.err, ERR_TIMEOUT, -2);
               break;
             }

@@ -70,6 +70,13 @@ struct DecodeParams {
   // (any other contents read as zero): the last CTA to finish its part of a
   // segment merges the segment's partials
   unsigned long long* seg_count;
+  // Limit (ns) of a CTA's wait for the other parts of a cut segment (0: the
+  // default limit of every bounded wait), and parts added to every cut
+  // segment's expected count.  Both are 0 in every public call; the
+  // wait-expiry test hook (pa_testing_decode_part_wait) sets them so that the
+  // wait runs out within a short limit.
+  unsigned long long part_wait_ns;
+  int32_t test_extra_parts;
   int32_t heads_per_box;  // HB: KV heads loaded per TMA box (power of two <= 8)
   int32_t smem_budget;    // dynamic shared memory the stage ring is sized against
   int32_t batch;
@@ -119,10 +126,11 @@ bool encode_pool_tmap(CUtensorMap* map, const void* base, int64_t rows, int num_
 bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
                               int box_blocks);
 // An e4m3 pool as a 3-D tensor {head_dim codes, slots, heads}: one box
-// {head_dim, box_rows, box_heads} lands as [head][row][head_dim B], each row's
-// 16-byte chunks swizzled (128-byte swizzle for head_dim 128, 64-byte for 64).
+// {head_dim, box_rows, box_heads} lands as [head][row][head_dim B], with
+// `swizzle` each row's 16-byte chunks swizzled (128-byte swizzle for head_dim
+// 128, 64-byte for 64), else rows plainly one after another.
 bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
-                         int box_rows, int box_heads);
+                         int box_rows, int box_heads, bool swizzle);
 
 // ---- prefill (bf16) ------------------------------------------------------
 struct PrefillParams {
@@ -153,6 +161,10 @@ struct PrefillParams {
   int32_t batch_rows;
   int32_t prefix_len;
   int32_t chunk_tiles;
+  // e4m3 pools: K/V codes, k_scale folded into scale_log2 on the host, every
+  // output row multiplied by v_scale (1 for bf16 pools)
+  int32_t kv8;
+  float v_scale;
 };
 cudaError_t launch_prefill_bf16(const PrefillParams& p, cudaStream_t s);
 

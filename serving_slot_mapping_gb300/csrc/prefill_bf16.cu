@@ -35,6 +35,13 @@
 //   updated reference max (O and l are rescaled in TMEM only when the row
 //   max grows by more than 2^8), and at the end write O / l as bf16.
 // Fully masked key tiles are never loaded or multiplied.
+//
+// e4m3 pools (KV8): the TMA lands each page's codes ([keys][D B], unswizzled)
+// in the upper half of the K or V ring slot, and an eleventh warp converts the
+// tile in place into the f16 layout above (cvt e4m3x2 -> f16x2 is exact:
+// every e4m3 value is an f16), zeroing rows at or past L_b.  Q is staged and P
+// written as f16, so both products are kind::f16 with f16 operands; k_scale is
+// folded into the softmax scale and v_scale into the final normalisation.
 #include <math.h>
 
 #include "common.cuh"
@@ -53,15 +60,16 @@ constexpr int kNSK = 3;              // K ring stages
 constexpr int kNSV = 2;              // V ring stages
 constexpr int kMmaWarp = 8;          // warps 0..7: softmax of query tile (warp / 4)
 constexpr int kTmaWarp = 9;
-// 10 warps: 3 on two SM sub-partitions, so at most 168 registers a thread;
-// the softmax holds half a row of S (64 fp32) at a time
-constexpr int kThreads = 32 * 10;
+constexpr int kCvtWarp = 10;         // e4m3 pools: converts landed code tiles to f16
+// 10 warps (11 for e4m3 pools): at most 3 on an SM sub-partition, so at most
+// 168 registers a thread; the softmax holds half a row of S (64 fp32) at a time
 constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row Q tile (16 KB)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kBarSlots = 24;
 
-template <int D>
+template <int D, bool KV8 = false>
 struct PCfg {
+  static constexpr int kThreads = 32 * (KV8 ? 11 : 10);
   static constexpr int kSlabs = D / 64;
   static constexpr int kRowBlock = kSlabs * 1024;      // one 8-key block of a K/V tile, all slabs
   static constexpr int kQBytes = kSlabs * kSlab;       // one Q tile
@@ -83,16 +91,65 @@ struct PCfg {
 // its barrier: S_t(j+1) is issued only after PV_t(j), which needs P_t(j).
 // B_VLAST completes the copies of a last V tile that the TMA warp still has
 // to zero past L before publishing it.
+// e4m3 pools: K/V FULL means the codes landed, K/V READY that the converter
+// has written the f16 tile (the MMA waits for READY).
 enum { B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + kNSK, B_VFULL = B_KEMPTY + kNSK, B_VEMPTY = B_VFULL + kNSV,
        B_SFULL = B_VEMPTY + kNSV, B_PFULL = B_SFULL + kQT, B_ODONE = B_PFULL + kQT, B_VLAST = B_ODONE + kQT,
-       B_COUNT = B_VLAST + 1 };
+       B_KREADY = B_VLAST + 1, B_VREADY = B_KREADY + kNSK, B_COUNT = B_VREADY + kNSV };
 static_assert(B_COUNT <= kBarSlots, "barrier slots");
 
+// e4m3 pools: one warp turns the codes of a landed tile ([kBN keys][D B] in
+// the upper half of its ring slot) into f16 in the UMMA layout over the whole
+// slot ([8-key block][slab][8 keys][128 B], 128-byte swizzle), rows at or past
+// `valid` set to zero.  The 8-key blocks go in order, four at a time with all
+// loads of the four before any store: block k's f16 bytes overlay the codes of
+// blocks 2k - 16 and 2k - 15 only, which are converted by then or in the same
+// four.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void convert_tile_e4m3(unsigned char* slot, int valid, int lane) {
+  constexpr int kChunks = D / 16;            // 16-code chunks of one key's row
+  constexpr int kKeysPerLoad = 32 / kChunks;  // keys one warp-wide load covers (4 or 8)
+  constexpr int kLoads = 8 / kKeysPerLoad;    // loads per lane per 8-key block (2 or 1)
+  constexpr int kRowBlock = (D / 64) * 1024;  // bytes of one 8-key block in f16
+  const unsigned char* codes = slot + kBN * D;
+  const int m = lane % kChunks, r0 = lane / kChunks;
+#pragma unroll 1
+  for (int k0 = 0; k0 < kBN / 8; k0 += 4) {
+    uint4 raw[4][kLoads];
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+      for (int x = 0; x < kLoads; ++x)
+        raw[kb][x] = *reinterpret_cast<const uint4*>(codes + ((k0 + kb) * 8 + r0 + x * kKeysPerLoad) * D + m * 16);
+    __syncwarp();
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+      for (int x = 0; x < kLoads; ++x) {
+        const int key = (k0 + kb) * 8 + r0 + x * kKeysPerLoad, kr = key & 7;
+        const uint4 w = raw[kb][x];
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;  // dims 16m .. 16m+7 and 16m+8 .. 16m+15
+        if (key < valid) {
+          lo = make_uint4(e4m3x2_lo_to_f16x2(w.x), e4m3x2_hi_to_f16x2(w.x), e4m3x2_lo_to_f16x2(w.y),
+                          e4m3x2_hi_to_f16x2(w.y));
+          hi = make_uint4(e4m3x2_lo_to_f16x2(w.z), e4m3x2_hi_to_f16x2(w.z), e4m3x2_lo_to_f16x2(w.w),
+                          e4m3x2_hi_to_f16x2(w.w));
+        }
+        unsigned char* blk = slot + (key >> 3) * kRowBlock + kr * 128;
+        const int c0 = 2 * m, c1 = 2 * m + 1;  // 8-dim chunks over D
+        *reinterpret_cast<uint4*>(blk + (c0 >> 3) * 1024 + (((c0 & 7) ^ kr) << 4)) = lo;
+        *reinterpret_cast<uint4*>(blk + (c1 >> 3) * 1024 + (((c1 & 7) ^ kr) << 4)) = hi;
+      }
+    __syncwarp();
+  }
+}
+
+template <int D, bool KV8>
+__global__ void __launch_bounds__(PCfg<D, KV8>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                       PrefillParams p) {
-  using C = PCfg<D>;
+  using C = PCfg<D, KV8>;
+  constexpr int kThreads = C::kThreads;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -182,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_ODONE + t), 1);
     }
     mbar_init(bar(B_VLAST), 1);
+    for (int s = 0; s < kNSK; ++s) mbar_init(bar(B_KREADY + s), 1);
+    for (int s = 0; s < kNSV; ++s) mbar_init(bar(B_VREADY + s), 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -202,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issued, and a V tile reuses the ids its K tile looked up.
     const int kpo = ps < kBN ? ps : kBN;  // keys per box
     const int ops = kBN / kpo;
-    const uint32_t box_bytes = (uint32_t)kpo * D * 2;
+    const uint32_t box_bytes = (uint32_t)kpo * D * (KV8 ? 1 : 2);
     const int32_t* bt = p.block_table + (pre ? 0 : page_list_start(p.kv_indptr, p.max_blocks, b));
     int* page_ring = reinterpret_cast<int*>(smem + C::kPageOff);
     auto fetch = [&](int j) {  // raw block_table entry of this lane's box in tile j, -1 if none
@@ -216,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (ok) {
         const int64_t slot = ((int64_t)page << pshift) + ((j * kBN + lane * kpo) & (ps - 1));
-        tma_load_5d(dst + (uint32_t)(lane * (kpo / 8)) * C::kRowBlock, map, 0, 0, 0, (int)(slot >> 3), hk, full);
+        if (KV8)  // codes in the slot's upper half, [keys][D B]
+          tma_load_3d(dst + (uint32_t)(kBN * D + lane * kpo * D), map, 0, (int)slot, hk, full);
+        else
+          tma_load_5d(dst + (uint32_t)(lane * (kpo / 8)) * C::kRowBlock, map, 0, 0, 0, (int)(slot >> 3), hk, full);
       }
     };
     auto slot_free = [&](int i) {  // lane 0 polls, the warp agrees
@@ -252,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int page = page_ring[(jv & 7) * 32 + lane];
         const uint32_t vdst = v_base + s * C::kKVTile;
         const int valid = L - jv * kBN;  // keys of this tile below L (>= 1)
-        if (valid >= kBN) {
+        if (KV8 || valid >= kBN) {  // (e4m3: the converter zeroes the rows past L)
           issue(&tmap_v, vdst, jv, page, bar(B_VFULL + s));
         } else {
           // last tile: slots valid..127 must hold zeros (they meet P = 0, and
@@ -289,6 +351,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
 
+  if (KV8 && warp == kCvtWarp) {
+    // ======================= e4m3 -> f16 converter (one warp) =======================
+    // Tiles in the order the MMA thread consumes them: K(j), V(j), K(j+1), ...
+    for (int j = jb; j < nt && alive; ++j) {
+      const int jl = j - jb, valid = min(L - j * kBN, kBN);
+      const int sk = jl % kNSK, sv = jl % kNSV;
+      alive = __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL + sk), (uint32_t)((jl / kNSK) & 1), p.err));
+      convert_tile_e4m3<D>(smem + C::kKOff + sk * C::kKVTile, valid, lane);
+      fence_proxy_async_smem();  // the f16 tile before the tensor core reads it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_KREADY + sk));
+      if (alive) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VFULL + sv), (uint32_t)((jl / kNSV) & 1), p.err));
+      convert_tile_e4m3<D>(smem + C::kVOff + sv * C::kKVTile, valid, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_VREADY + sv));
+    }
+  }
+
   if (warp == kMmaWarp && lane == 0) {
     // ======================= MMA issuer =======================
     // Fixed order S_A(0) S_B(0), then per key tile j: PV_A(j) S_A(j+1)
@@ -296,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two query tiles alternate on the tensor core, each one's softmax running
     // while the other's products do.  The first S of a key tile waits for K,
     // the first PV for V; the last S (PV) of a key tile frees its K (V) stage.
-    constexpr uint32_t idesc_s = umma_idesc_bf16(kBM, kBN, false);
-    constexpr uint32_t idesc_o = umma_idesc_bf16(kBM, D, true);
+    constexpr uint32_t idesc_s = KV8 ? umma_idesc_f16(kBM, kBN, false) : umma_idesc_bf16(kBM, kBN, false);
+    constexpr uint32_t idesc_o = KV8 ? umma_idesc_f16(kBM, D, true) : umma_idesc_bf16(kBM, D, true);
+    constexpr int kKWait = KV8 ? B_KREADY : B_KFULL, kVWait = KV8 ? B_VREADY : B_VFULL;
     // descriptors at the base of each operand; a K step adds its byte offset / 16
     // to the start-address field (every address stays below 256 KB, so no carry)
     const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s), 16, 1024);
@@ -309,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jl = j - jb;
       const int sk = jl % kNSK;
       if (t == 0 || j >= nt0) {  // first S of key tile j
-        if (alive) alive = mbar_wait(bar(B_KFULL + sk), (uint32_t)((jl / kNSK) & 1), p.err);
+        if (alive) alive = mbar_wait(bar(kKWait + sk), (uint32_t)((jl / kNSK) & 1), p.err);
         tc_fence_after();
       }
       const uint64_t qd = q_desc + (uint64_t)((t * C::kQBytes) >> 4);
@@ -327,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sv = jl % kNSV;
       if (alive) alive = mbar_wait(bar(B_PFULL + t), (uint32_t)(jl & 1), p.err);
       if (t == 0 || j >= nt0) {  // first PV of key tile j
-        if (alive) alive = mbar_wait(bar(B_VFULL + sv), (uint32_t)((jl / kNSV) & 1), p.err);
+        if (alive) alive = mbar_wait(bar(kVWait + sv), (uint32_t)((jl / kNSV) & 1), p.err);
       }
       tc_fence_after();
       const uint64_t vd = v_desc + (uint64_t)((sv * C::kKVTile) >> 4);
@@ -361,12 +443,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     {  // this thread's Q row into the UMMA A layout (K-major, 128-byte swizzle); zeros past the last row
       unsigned char* qt = q_s + t * C::kQBytes;
       const __nv_bfloat16* src = qp + (valid_row ? row_off(R) : 0);
+      if (KV8) {  // f16 operands: bf16 -> f16 on the way in
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (valid_row) {
+            v = __ldg(reinterpret_cast<const uint4*>(src) + c);
+            v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+          }
+          *reinterpret_cast<uint4*>(qt + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        }
+      } else {
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        cp_async_16(smem_u32(qt + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8,
-                    valid_row ? 16 : 0);
-      cp_async_commit();
-      cp_async_wait<0>();
+        for (int c = 0; c < D / 8; ++c)
+          cp_async_16(smem_u32(qt + (c >> 3) * kSlab + r * 128 + (((c & 7) ^ (r & 7)) << 4)), src + c * 8,
+                      valid_row ? 16 : 0);
+        cp_async_commit();
+        cp_async_wait<0>();
+      }
       fence_proxy_async_smem();
       mbar_arrive(bar(B_QFULL));
     }
@@ -450,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float p0 = fast_exp2(fmaf(__uint_as_float(v[cb][e]), sl2, -mbase));
               const float p1 = fast_exp2(fmaf(__uint_as_float(v[cb][e + 1]), sl2, -mbase));
               rs[(e >> 1) & 7] += p0 + p1;
-              w[cb * 16 + (e >> 1)] = pack_bf16(p0, p1);
+              w[cb * 16 + (e >> 1)] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
             }
         } else {
 #pragma unroll
@@ -460,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float p0 = fast_exp2(scaled(v[cb][e], h * 64 + cb * 32 + e) - mbase);
               const float p1 = fast_exp2(scaled(v[cb][e + 1], h * 64 + cb * 32 + e + 1) - mbase);
               rs[(e >> 1) & 7] += p0 + p1;
-              w[cb * 16 + (e >> 1)] = pack_bf16(p0, p1);
+              w[cb * 16 + (e >> 1)] = KV8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
             }
         }
         tmem_st32(s_col + h * 32, w);
@@ -510,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (valid_row) p.part_ml[pr] = make_float2(m_ref, l);
     }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? p.v_scale / l : 0.f;  // v_scale: 1 for bf16 pools
     __nv_bfloat16* orow = outp + (valid_row ? row_off(R) : 0);
 #pragma unroll
     for (int cb = 0; cb < D / 32 && !pre; ++cb) {
@@ -543,18 +637,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D>
+template <int D, bool KV8>
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
-  using C = PCfg<D>;
+  using C = PCfg<D, KV8>;
   const int ps = p.pool.page_size;
   if (ps < 8 || p.pool.page_shift < 0) return cudaErrorInvalidValue;
+  if (KV8 && p.part_o != nullptr) return cudaErrorInvalidValue;  // the cascade prefix pass: bf16 pools
   const int kpo = ps < kBN ? ps : kBN;  // keys per TMA box
   const int64_t rows = p.pool.num_pages * (int64_t)ps;
   CUtensorMap tk, tv;
-  if (!encode_pool_tmap_blocked(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, kpo / 8) ||
-      !encode_pool_tmap_blocked(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, kpo / 8))
+  if (KV8) {
+    if (!encode_pool_tmap_u8(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, kpo, 1, false) ||
+        !encode_pool_tmap_u8(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, kpo, 1, false))
+      return cudaErrorInvalidValue;
+  } else if (!encode_pool_tmap_blocked(&tk, p.pool.key_pool, rows, p.pool.num_kv_heads, D, kpo / 8) ||
+             !encode_pool_tmap_blocked(&tv, p.pool.value_pool, rows, p.pool.num_kv_heads, D, kpo / 8)) {
     return cudaErrorInvalidValue;
-  auto kern = prefill_tc_kernel<D>;
+  }
+  auto kern = prefill_tc_kernel<D, KV8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = ((int64_t)p.max_q_len * p.group + kQT * kBM - 1) / (kQT * kBM);
@@ -564,7 +664,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
     const int nt = (p.prefix_len + kBN - 1) / kBN;
     gz = (unsigned)((nt + p.chunk_tiles - 1) / p.chunk_tiles);
   }
-  return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, gz), dim3(kThreads),
+  return launch_pdl(kern, dim3((unsigned)tiles, (unsigned)p.pool.num_kv_heads, gz), dim3(C::kThreads),
                     (size_t)C::kSmem, s, tk, tv, p);
 }
 
@@ -572,7 +672,8 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t s) {
 
 cudaError_t launch_prefill_bf16(const PrefillParams& p, cudaStream_t s) {
   if (p.max_q_len <= 0 || p.batch <= 0) return cudaSuccess;
-  return p.pool.head_dim == 128 ? launch_prefill_tc<128>(p, s) : launch_prefill_tc<64>(p, s);
+  if (p.kv8) return p.pool.head_dim == 128 ? launch_prefill_tc<128, true>(p, s) : launch_prefill_tc<64, true>(p, s);
+  return p.pool.head_dim == 128 ? launch_prefill_tc<128, false>(p, s) : launch_prefill_tc<64, false>(p, s);
 }
 
 }  // namespace pa

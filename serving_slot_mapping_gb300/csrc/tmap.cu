@@ -67,7 +67,7 @@ bool encode_pool_tmap_blocked(CUtensorMap* map, const void* base, int64_t rows, 
 }
 
 bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int num_kv_heads, int head_dim,
-                         int box_rows, int box_heads) {
+                         int box_rows, int box_heads, bool swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)rows, (cuuint64_t)num_kv_heads};
@@ -77,7 +77,8 @@ bool encode_pool_tmap_u8(CUtensorMap* map, const void* base, int64_t rows, int n
   // a row of head_dim codes is one swizzle span: 128-byte rows (head_dim 128)
   // take the 128-byte swizzle, 64-byte rows the 64-byte one
   if (head_dim != 64 && head_dim != 128) return false;
-  const CUtensorMapSwizzle sw = head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle sw = !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                         : (head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

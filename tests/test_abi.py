@@ -136,8 +136,11 @@ def test_e4m3_pool_validation(L):
     assert L.paged_attention_decode_workspace_size(4, 32, 8, 128, f8) == \
         L.paged_attention_decode_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_BF16)
     p = _pool(dtype=f8)
-    assert L.paged_attention_prefill(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4,
-                                     FAKE, 64, 0.1, None) == capi.PA_ERR_UNSUPPORTED  # decode and append only
+    # prefill on an e4m3 pool reads q rows 16 bytes at a time
+    assert L.paged_attention_prefill(ctypes.byref(p), ctypes.c_void_p(0x40008), ctypes.c_void_p(0x50000), 2, 32,
+                                     FAKE, 10, 5, FAKE, 4, FAKE, 64, 0.1, None) == capi.PA_ERR_ALIGN
+    assert L.paged_attention_prefill(ctypes.byref(_pool(dtype=f8, ks=-1.0)), FAKE, ctypes.c_void_p(0x50000), 2,
+                                     32, FAKE, 10, 5, FAKE, 4, FAKE, 64, 0.1, None) == capi.PA_ERR_RANGE
     assert _decode(L, _pool(dtype=3)) == capi.PA_ERR_DTYPE
 
 
@@ -158,3 +161,22 @@ def test_decode_append_validation(L):
     assert call(hq=12) == capi.PA_ERR_SHAPE
     assert call(scale=float("nan")) == capi.PA_ERR_RANGE
     assert call() == capi.PA_ERR_WORKSPACE                               # bf16 needs the decode workspace
+
+
+def test_part_wait_hook_validation(L):
+    """The wait-expiry test hook can only shorten a wait: limits outside
+    1 us .. 2 s, negative or huge part counts and f32 pools are refused
+    before any launch."""
+    f = L.pa_testing_decode_part_wait
+    p = _pool()
+
+    def call(pool=p, wait_ns=1_000_000, extra=1, ws=FAKE, wsb=1 << 30):
+        return f(ctypes.byref(pool), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 4, FAKE, 64, 0.1, ws, wsb,
+                 wait_ns, extra, None)
+    assert call(wait_ns=999) == capi.PA_ERR_RANGE
+    assert call(wait_ns=2_000_000_001) == capi.PA_ERR_RANGE
+    assert call(extra=-1) == capi.PA_ERR_RANGE
+    assert call(extra=1025) == capi.PA_ERR_RANGE
+    assert call(pool=_pool(dtype=capi.PA_DTYPE_F32)) == capi.PA_ERR_UNSUPPORTED
+    assert call(ws=None, wsb=0) == capi.PA_ERR_WORKSPACE
+    assert f(None, FAKE, FAKE, 2, 32, FAKE, 4, FAKE, 64, 0.1, FAKE, 1, 1_000_000, 1, None) == capi.PA_ERR_NULL

@@ -91,3 +91,61 @@ def test_cascade_close_to_plain_decode_over_full_tables(cuda_device):
     torch.cuda.synchronize()
     diff = (out.float() - ref.float()).abs()
     assert diff.max().item() <= 2e-2 and diff.mean().item() <= 2e-3
+
+
+def test_cascade_large_batch(cuda_device):
+    """640 sequences (10 tiles of 256 query rows per KV head in the prefix
+    pass); own parts are ragged, some sequences have none."""
+    rng = np.random.RandomState(7)
+    own = rng.randint(0, 40, size=640).tolist()
+    plan = _plan("casc_large", 32, 8, 128, 16, 9, own, seed=12)
+    _run(plan, cuda_device, 9, 9 * 16 - 3, "cascade, large batch")
+
+
+def test_cascade_many_short_and_empty_own_parts(cuda_device):
+    """Many segments of a few blocks each; a third of the sequences have no
+    key of their own (their rows come from the prefix alone)."""
+    rng = np.random.RandomState(8)
+    own = rng.randint(1, 20, size=150).tolist()
+    for b in range(0, 150, 3):
+        own[b] = 0
+    plan = _plan("casc_short", 16, 4, 128, 16, 30, own, seed=13)
+    _run(plan, cuda_device, 30, 30 * 16, "cascade, short own parts")
+
+
+def test_cascade_graph_replays_on_a_garbage_workspace(cuda_device):
+    """A workspace filled with random bytes, then CUDA graph replays with new
+    queries: every replay must recompute and merge all partials."""
+    plan = wl.shared_prefix_plan(batch=24, prefix_pages=40, unique_pages=6, seed=15)
+    st = wl.materialize(plan, cuda_device)
+    kp, vp = st.key_pool.clone(), st.value_pool.clone()
+    capi.paged_kv_append(kp, vp, st.key, st.value, st.slot_mapping)
+    pre, plen, own_bt, own_lens = wl.cascade_tables(plan, 40, 40 * plan.page_size)
+    dev = lambda a: torch.from_numpy(a).to(cuda_device)
+    pre_t, bt_t, sl_t = dev(pre), dev(own_bt), dev(own_lens)
+    ws = capi.cascade_workspace(plan.batch, plan.num_q_heads, kp)
+    ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, generator=torch.Generator().manual_seed(2)))
+    q = st.q.clone()
+    out = torch.full_like(q, float("nan"))
+    s = torch.cuda.Stream()
+
+    def call():
+        capi.paged_attention_decode_cascade(kp, vp, q, pre_t, plen, bt_t, sl_t, plan.scale,
+                                            max_seq_len=int(own_lens.max()), out=out, workspace=ws, stream=s)
+    with torch.cuda.stream(s):
+        call()                        # eager first: the first cascade call on a thread precedes any capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    kb, vb = bits(kp), bits(vp)
+    for rep in range(3):
+        q.copy_(torch.randn(q.shape, generator=torch.Generator().manual_seed(30 + rep)).to(q.dtype))
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        exp = oracle.paged_attention_decode_cascade(to_f64(kb), to_f64(vb), to_f64(bits(q)), pre, plen, own_bt,
+                                                    own_lens, plan.scale)
+        assert_close(out, exp, "bf16", f"cascade graph replay {rep}")

@@ -50,10 +50,9 @@ def test_fp8_append_and_decode(cuda_device, name):
                                       max_seq_len=int(plan.seq_lens.max()), k_scale=KS, v_scale=VS)
     torch.cuda.synchronize()
     assert capi.device_error() == (0, 0)
-    seqs = list(range(plan.batch)) if plan.batch <= 32 else list(range(0, plan.batch, 4))
     exp = kv_fp8.paged_attention_decode_fp8(kc, vc, KS, VS, to_f64(bits(st.q)), plan.block_table, plan.seq_lens,
-                                            plan.scale, seqs=seqs)
-    assert_close(out, exp, "bf16", f"fp8 decode {name}", rows=seqs)
+                                            plan.scale)
+    assert_close(out, exp, "bf16", f"fp8 decode {name}")   # every sequence
 
 
 @pytest.mark.parametrize("hq,hkv,d,ps", [(32, 1, 128, 16), (16, 4, 64, 8), (8, 8, 128, 64), (32, 8, 64, 16)])
@@ -81,8 +80,12 @@ def test_fp8_decode_csr_and_static_scratch_match(cuda_device):
     ip, ix, last = (torch.from_numpy(x).to(cuda_device) for x in wl.csr_tables(plan))
     b = capi.paged_attention_decode_csr(kp, vp, st.q, ip, ix, last, plan.scale, max_seq_len=msl,
                                         k_scale=KS, v_scale=VS)
+    c = capi.paged_attention_decode_static_scratch(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                                   max_seq_len=msl, k_scale=KS, v_scale=VS)
     torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
 def test_fp8_quantiser_saturates_and_keeps_nan(cuda_device):
@@ -99,3 +102,67 @@ def test_fp8_quantiser_saturates_and_keeps_nan(cuda_device):
     got = _codes(kp).reshape(P * ps, hkv, d)[[5, 17, 40]]
     assert np.array_equal(got, exp)
     assert (got == 0x7E).any() and (got == 0xFE).any() and (got == 0x7F).any()
+
+
+# ---------------------------------------------------------------------------
+# prefill over e4m3 pools
+# ---------------------------------------------------------------------------
+
+def _fp8_prefill(plan, device, ks=KS, vs=VS, rows=None):
+    """Quantising append of the new rows, then prefill; (out, expected, codes ok)."""
+    kp, vp, kc, vc, st = _fp8_step(plan, device, ks, vs)
+    assert np.array_equal(_codes(kp), kc) and np.array_equal(_codes(vp), vc)   # append: every byte
+    out = capi.paged_attention_prefill(kp, vp, st.q, st.query_start_loc, st.block_table, st.seq_lens,
+                                       plan.scale, max_q_len=int(plan.new.max()),
+                                       max_seq_len=int(plan.seq_lens.max()), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    q = to_f64(bits(st.q))
+    exp = np.zeros(q.shape)
+    qsl = plan.query_start_loc
+    for b in range(plan.batch):   # 256 rows at a time bounds the oracle's memory
+        for r0 in range(int(qsl[b]), int(qsl[b + 1]), 256):
+            rr = list(range(r0, min(r0 + 256, int(qsl[b + 1]))))
+            exp[rr] = kv_fp8.paged_attention_prefill_fp8(kc, vc, ks, vs, q, qsl, plan.block_table,
+                                                         plan.seq_lens, plan.scale, rows=rr)[rr]
+    return out, exp, (kp, vp, st)
+
+
+def test_fp8_prefill_chunked_full_every_row(cuda_device):
+    """The mixed chunked-prefill workload (8 sequences, 10,496 new rows after
+    cached contexts up to 8192) on e4m3 pools: every row against the oracle."""
+    plan = wl.chunked_prefill_plan()
+    out, exp, _ = _fp8_prefill(plan, cuda_device)
+    assert_close(out, exp, "bf16", "fp8 chunked prefill, every row")
+
+
+def test_fp8_prefill_tiny_shape(cuda_device):
+    """The tiny workload's shape (one sequence, 4 query / 2 KV heads, head_dim
+    64, page 16, 7 of 64 pages) prefilled on an e4m3 pool."""
+    rng = np.random.RandomState(0)
+    pages = list(rng.choice(64, 7, replace=False))
+    plan = wl._assemble("tiny_fp8_prefill", "prefill", "bf16", 4, 2, 64, 16, [0], [100], [pages], 64,
+                        1.0 / 8.0, 0)
+    out, exp, _ = _fp8_prefill(plan, cuda_device, ks=0.05, vs=0.01)
+    assert_close(out, exp, "bf16", "fp8 tiny prefill")
+
+
+@pytest.mark.parametrize("hq,hkv,d,ps", [(32, 8, 128, 16), (8, 1, 128, 8), (4, 4, 64, 32), (32, 1, 64, 64),
+                                         (16, 4, 128, 256)])
+def test_fp8_prefill_ragged(cuda_device, hq, hkv, d, ps):
+    plan = wl.chunked_prefill_plan(new=(1, 7, 16, 65, 130, 3, 300), cached=(0, 9, 100, 0, 31, 500, 127),
+                                   seed=hq + hkv + d + ps, hq=hq, hkv=hkv, d=d, ps=ps)
+    out, exp, _ = _fp8_prefill(plan, cuda_device, ks=0.04, vs=0.02)
+    assert_close(out, exp, "bf16", f"fp8 prefill {hq}/{hkv}/{d} ps{ps}")
+
+
+def test_fp8_prefill_csr_matches_row_padded(cuda_device):
+    plan = wl.chunked_prefill_plan(new=(40, 200, 3), cached=(17, 0, 900), seed=44)
+    out, exp, (kp, vp, st) = _fp8_prefill(plan, cuda_device)
+    assert_close(out, exp, "bf16", "fp8 prefill (row-padded)")
+    ip, ix, last = (torch.from_numpy(x).to(cuda_device) for x in wl.csr_tables(plan))
+    out2 = capi.paged_attention_prefill_csr(kp, vp, st.q, st.query_start_loc, ip, ix, last, plan.scale,
+                                            max_q_len=int(plan.new.max()), max_seq_len=int(plan.seq_lens.max()),
+                                            k_scale=KS, v_scale=VS)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))

@@ -1,16 +1,25 @@
 """GPU checks of the split-KV merge inside the decode kernel.
 
 A segment (one sequence's keys for one box of KV heads) whose 16-key blocks
-are cut across CTAs is finished by whichever CTA completes its last part: the
-CTAs count their parts in workspace words tagged with the launch's grid id,
-and the last one merges every part's (m, l, o) with the combine identity
-(mobius PR #395 "Add paged / block-table KV cache export": the decode output
-is softmax attention over all seq_lens[b] keys, which the merge reassembles
-exactly up to rounding).  So the workspace needs no initialisation, and every
-launch -- eager or a CUDA graph replay -- must merge afresh.  Each case below
-changes the inputs between launches, so a launch that skipped its merge would
-leave a stale or zero output and fail against the oracle.
+are cut across CTAs leaves one fp32 partial (m, l, o) per CTA.  Each CTA
+counts its part on a per-segment word tagged with a per-launch epoch (kept at
+the workspace's start), and after its own range every CTA that holds a part
+waits -- bounded -- until all parts are counted and merges a slice of the
+segment's rows with the combine identity (mobius PR #395 "Add paged /
+block-table KV cache export": the decode output is softmax attention over all
+seq_lens[b] keys, which the merge reassembles exactly up to rounding).  The
+grid is launched cooperatively so that all its CTAs are resident; without
+that launch the CTA that counts a segment's last part merges all of it.  So
+the workspace needs no initialisation, and every launch -- eager or a CUDA
+graph replay -- must merge afresh.  Each case below changes the inputs
+between launches, so a launch that skipped its merge would leave a stale or
+NaN output and fail against the oracle.  The last case makes the bounded
+wait run out (through the library's test hook) and checks that the kernel
+reports it and returns.
 """
+import ctypes
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -191,3 +200,39 @@ def test_merge_without_cooperative_launch():
                          timeout=600, cwd=root)
     assert out.returncode == 0, (out.stdout[-1500:], out.stderr[-3000:])
     assert "fallback merge ok" in out.stdout
+
+
+def test_bounded_part_wait_runs_out_and_is_reported(cuda_device):
+    """The decode kernel's one wait on other CTAs (a CTA holding part of a cut
+    segment waits for the other parts before merging its slice) is bounded.
+    Through the test hook every cut segment expects one part that never
+    arrives and the limit is 1 ms: the call must return within a few ms
+    instead of hanging, record code 5 (a bounded wait gave up, detail -2 =
+    the part wait) in the device error word, and leave the context usable --
+    a normal decode on the same workspace afterwards matches the oracle."""
+    plan = wl.gqa_decode_plan(batch=32, seed=23)      # ~145 blocks a sequence over 152 CTAs: all cut
+    st, kp, vp = _appended(plan, cuda_device)
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+    capi.device_error()
+    pool = capi.make_pool(kp, vp)
+    out = torch.full_like(st.q, float("nan"))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    status = capi.lib().pa_testing_decode_part_wait(
+        ctypes.byref(pool), ctypes.c_void_p(st.q.data_ptr()), ctypes.c_void_p(out.data_ptr()), plan.batch,
+        plan.num_q_heads, ctypes.c_void_p(st.block_table.data_ptr()), plan.max_blocks,
+        ctypes.c_void_p(st.seq_lens.data_ptr()), int(plan.seq_lens.max()), plan.scale,
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), 1_000_000, 1, stream)
+    assert status == capi.PA_OK
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert capi.device_error() == (5, -2)
+    assert elapsed < 1.0, f"the 1 ms part wait took {elapsed:.3f} s"
+    # the same workspace, a normal call: unaffected
+    for rep in range(2):
+        q = _new_q(st.q, 90 + rep)
+        got = _decode(st, kp, vp, q, ws)
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        assert_close(got, _expect(st, kp, vp, q), "bf16", f"decode after an expired wait, rep {rep}")
