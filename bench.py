@@ -12,8 +12,8 @@ long-context decode, 256 sequences with contexts U[1024, 32768], 32 query /
 Inputs are synthetic, seeded, and resident in HBM; the L2 is flushed (256 MB
 write, then 256 MB read of another buffer, both untimed) between timed
 steps.  `value` is the decode KV-read throughput of the whole job: the
-algorithmic K+V bytes every rank's step must read, divided by the median
-step time (max over ranks).
+algorithmic K+V bytes every rank's step must read, divided by the mean step
+time (max over ranks).
 
 --impl reference times the fp64 CPU oracle (the only reference there is) on
 the host cores, on a bounded sample of the same workload.
@@ -135,15 +135,15 @@ def file_hash(*paths):
 
 def repeatability(times, repeats=5, limit=1.05):
     """The timed steps cut into ``repeats`` consecutive runs: the median of the
-    runs' median step times, their spread (slowest / fastest run) and whether
-    the spread is within ``limit`` (a number whose runs disagree by more is
-    flagged as not reportable)."""
+    runs' mean step times, their spread (slowest / fastest run) and whether the
+    spread is within ``limit`` (a number whose runs disagree by more is flagged
+    as not reportable)."""
     times = [float(t) for t in times]
     k = max(1, min(repeats, len(times)))
     if not times:
         return {"repeats": 0, "median_ms": None, "spread": None, "reportable": False}
     size = len(times) // k
-    runs = [statistics.median(times[i * size:(i + 1) * size if i < k - 1 else len(times)]) for i in range(k)]
+    runs = [statistics.mean(times[i * size:(i + 1) * size if i < k - 1 else len(times)]) for i in range(k)]
     spread = max(runs) / min(runs) if min(runs) > 0 else None
     return {"repeats": k, "median_ms": round(statistics.median(runs), 5),
             "spread": round(spread, 4) if spread is not None else None,
@@ -479,7 +479,7 @@ def e2e_decode(rig: DecodeRig, steps, flush):
         one()
         e.record(stream)
     torch.cuda.synchronize()
-    ms = statistics.median(s.elapsed_time(e) for s, e in ev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
     return ms, h2d, d2h
 
 
@@ -704,13 +704,13 @@ def run_ours(args, rank, world, local):
     # repeatability of the step on runs long enough to mean something
     rep_times = timed_graph(g_step, REPEAT_RUNS * REPEAT_REPLAYS, flush, stream)
 
-    ms_step = max_over_ranks(statistics.median(times), world)
+    ms_step = max_over_ranks(statistics.mean(times), world)
     kv_bytes = rig.kv_bytes()
     total_kv = sum_over_ranks(float(kv_bytes), world)
     value = total_kv / (ms_step * 1e-3) / 1e9
     tokens_s = sum_over_ranks(float(plan.batch), world) / (ms_step * 1e-3)
 
-    dec_ms = statistics.median(dec_times)
+    dec_ms = statistics.mean(dec_times)
     # algorithmic bytes of the attention call: cascade reads the shared prefix once
     unique = wl.decode_unique_kv_bytes(plan) if args.decode == "cascade" else None
     dec_bytes = (unique if unique is not None else kv_bytes) + wl.decode_io_bytes(plan)
@@ -747,7 +747,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "ms_per_step_mean": round(max_over_ranks(statistics.mean(times), world), 5),
+        "ms_per_step_median": round(max_over_ranks(statistics.median(times), world), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 KV, f16 products" if rig.kv8 else "bf16",
         "data": "synthetic",
@@ -760,7 +760,8 @@ def run_ours(args, rank, world, local):
                    "unique_kv_bytes_per_step": wl.decode_unique_kv_bytes(plan) // (2 if rig.kv8 else 1),
                    "step": "append 1 token/seq + decode" + (" (one call)" if args.decode == "fused" else ""),
                    "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)",
-                   "timing": "median of the timed steps (CUDA events, one graph replay each)",
+                   "timing": "mean of the timed steps (CUDA events, one graph replay each; the event "
+                             "clock ticks in ~2 us steps, which a mean averages out and a median does not)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_hbm_peak": round(100.0 * value / (hbm * world), 2),
@@ -810,7 +811,7 @@ def e2e_prefill(rig, steps, flush):
         one()
         e_.record(stream)
     torch.cuda.synchronize()
-    return statistics.median(s_.elapsed_time(e_) for s_, e_ in ev), h2d, d2h
+    return statistics.mean(s_.elapsed_time(e_) for s_, e_ in ev), h2d, d2h
 
 
 def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, bf16_sus, peak_src):
@@ -832,11 +833,11 @@ def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, b
     pf_times = timed_graph(g_pf, max(20, args.steps), flush, stream)
     clocks = sampler.stop()
     rep_times = timed_graph(g_step, REPEAT_RUNS * REPEAT_REPLAYS, flush, stream)
-    ms_step = max_over_ranks(statistics.median(times), world)
+    ms_step = max_over_ranks(statistics.mean(times), world)
     flops = wl.prefill_flops(plan)
     total_flops = sum_over_ranks(float(flops), world)
     value = total_flops / (ms_step * 1e-3) / 1e12
-    pf_ms = statistics.median(pf_times)
+    pf_ms = statistics.mean(pf_times)
     achieved = flops / (pf_ms * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
@@ -850,7 +851,7 @@ def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, b
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "ms_per_step_mean": round(max_over_ranks(statistics.mean(times), world), 5),
+        "ms_per_step_median": round(max_over_ranks(statistics.median(times), world), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
@@ -859,7 +860,7 @@ def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, b
                    "visible_pairs": wl.prefill_visible_pairs(plan), "flops_per_step": flops,
                    "step": "append new tokens + varlen causal prefill",
                    "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)",
-                   "timing": "median of the timed steps (CUDA events, one graph replay each)"},
+                   "timing": "mean of the timed steps (CUDA events, one graph replay each)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16, 4), "traffic": traffic_for(f"prefill:{plan.name}"),
                      "kernel": "paged_attention_prefill (prefill_tc_kernel)", "ms_per_launch": round(pf_ms, 5),
@@ -881,7 +882,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             plan = wl.named_plan(name)
             rig = DecodeRig(plan, dev)
             g = capture(rig.decode, stream)
-            ms = statistics.median(timed_graph(g, max(steps, 100), flush, stream))
+            ms = statistics.mean(timed_graph(g, max(steps, 100), flush, stream))
             kvb = wl.decode_kv_bytes(plan)
             io = wl.decode_io_bytes(plan)
             gbs = (kvb + io) / (ms * 1e-3) / 1e9
@@ -907,7 +908,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
                         rig.st.key_pool, rig.st.value_pool, rig.st.q, pre_t, plen, bt_t, sl_t,
                         plan.scale, max_seq_len=msl, out=rig.out, workspace=cw)
                 gc = capture(cascade, stream)
-                cms = statistics.median(timed_graph(gc, max(steps, 100), flush, stream))
+                cms = statistics.mean(timed_graph(gc, max(steps, 100), flush, stream))
                 ent["cascade_ms"] = round(cms, 5)
                 ent["cascade_unique_GBps"] = round(ub / (cms * 1e-3) / 1e9, 1)
                 ent["cascade_unique_frac_hbm"] = round(ub / (cms * 1e-3) / 1e9 / hbm, 4)
@@ -923,7 +924,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             plan = wl.named_plan(name)
             rig = DecodeRig(plan, dev, "e4m3")
             g = capture(rig.decode, stream)
-            ms = statistics.median(timed_graph(g, steps, flush, stream))
+            ms = statistics.mean(timed_graph(g, steps, flush, stream))
             kvb = wl.decode_kv_bytes(plan) // 2 + wl.decode_io_bytes(plan)
             res[name + "_fp8"] = {"decode_ms": round(ms, 5), "kv_GBps": round(kvb / (ms * 1e-3) / 1e9, 1),
                                   "frac_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4),
@@ -933,7 +934,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             if bf is None:  # long_gqa is the main line: time its bf16 decode here too
                 rig16 = DecodeRig(plan, dev)
                 g16 = capture(rig16.decode, stream)
-                bf = statistics.median(timed_graph(g16, steps, flush, stream))
+                bf = statistics.mean(timed_graph(g16, steps, flush, stream))
                 del rig16, g16
                 torch.cuda.empty_cache()
             res[name + "_fp8"]["bf16_pool_decode_ms"] = round(bf, 5)
@@ -948,8 +949,8 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             rig = DecodeRig(plan, dev)
             g2 = capture(rig.step, stream)
             g1 = capture(rig.fused_step, stream)
-            ms2 = statistics.median(timed_graph(g2, steps, flush, stream))
-            ms1 = statistics.median(timed_graph(g1, steps, flush, stream))
+            ms2 = statistics.mean(timed_graph(g2, steps, flush, stream))
+            ms1 = statistics.mean(timed_graph(g1, steps, flush, stream))
             kvb = wl.decode_kv_bytes(plan)
             res[name + "_fused_step"] = {"step_ms": round(ms1, 5), "two_call_step_ms": round(ms2, 5),
                                          "kv_GBps": round(kvb / (ms1 * 1e-3) / 1e9, 1),
@@ -970,7 +971,7 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             rig.capi.paged_attention_decode_csr(rig.st.key_pool, rig.st.value_pool, rig.st.q, ip, ix, last,
                                                 plan.scale, max_seq_len=msl, out=rig.out, workspace=rig.ws)
         g = capture(decode_csr, stream)
-        ms = statistics.median(timed_graph(g, max(steps, 100), flush, stream))
+        ms = statistics.mean(timed_graph(g, max(steps, 100), flush, stream))
         kvb = wl.decode_kv_bytes(plan) + wl.decode_io_bytes(plan)
         res["gqa_decode_csr"] = {"decode_ms": round(ms, 5), "kv_GBps": round(kvb / (ms * 1e-3) / 1e9, 1),
                                  "frac_hbm": round(kvb / (ms * 1e-3) / 1e9 / hbm, 4)}
@@ -981,9 +982,9 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
         plan = wl.named_plan("chunked_prefill")
         rig = PrefillRig(plan, dev)
         g = capture(rig.prefill, stream)
-        ms = statistics.median(timed_graph(g, steps, flush, stream))
+        ms = statistics.mean(timed_graph(g, steps, flush, stream))
         ga = capture(rig.append, stream)
-        ams = statistics.median(timed_graph(ga, max(steps, 100), flush, stream))
+        ams = statistics.mean(timed_graph(ga, max(steps, 100), flush, stream))
         fl = wl.prefill_flops(plan)
         tf = fl / (ms * 1e-3) / 1e12
         ab = wl.append_bytes(plan)
