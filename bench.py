@@ -427,24 +427,36 @@ class DecodeRig:
 
 
 class PrefillRig:
-    def __init__(self, plan, dev):
+    """Device-resident prefill workload (bf16 pools, or e4m3 pools with one
+    scale per pool and tensor): a step appends the new rows and prefills."""
+
+    E4M3_SCALE = 0.02
+
+    def __init__(self, plan, dev, kv_dtype="bf16"):
         from serving_slot_mapping_gb300 import capi
         self.capi = capi
         self.plan = plan
         self.st = wl.materialize(plan, dev)
+        self.kv8 = kv_dtype == "e4m3"
+        self.ks = self.vs = self.E4M3_SCALE if self.kv8 else 1.0
+        if self.kv8:
+            self.st.key_pool = to_e4m3(self.st.key_pool, self.ks)
+            self.st.value_pool = to_e4m3(self.st.value_pool, self.vs)
         self.out = torch.empty_like(self.st.q)
         self.mql = int(plan.new.max())
         self.msl = int(plan.seq_lens.max())
 
     def append(self):
         st = self.st
-        self.capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping)
+        self.capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping,
+                                  k_scale=self.ks, v_scale=self.vs)
 
     def prefill(self):
         st = self.st
         self.capi.paged_attention_prefill(st.key_pool, st.value_pool, st.q, st.query_start_loc,
                                           st.block_table, st.seq_lens, self.plan.scale,
-                                          max_q_len=self.mql, max_seq_len=self.msl, out=self.out)
+                                          max_q_len=self.mql, max_seq_len=self.msl, out=self.out,
+                                          k_scale=self.ks, v_scale=self.vs)
 
     def step(self):
         self.append()
@@ -794,10 +806,11 @@ def e2e_prefill(rig, steps, flush):
     def one():
         for n in host:
             dev[n].copy_(host[n], non_blocking=True)
-        c.paged_kv_append(st.key_pool, st.value_pool, dev["key"], dev["value"], dev["slot_mapping"])
+        c.paged_kv_append(st.key_pool, st.value_pool, dev["key"], dev["value"], dev["slot_mapping"],
+                          k_scale=rig.ks, v_scale=rig.vs)
         c.paged_attention_prefill(st.key_pool, st.value_pool, dev["q"], dev["query_start_loc"],
                                   dev["block_table"], dev["seq_lens"], p.scale, max_q_len=rig.mql,
-                                  max_seq_len=rig.msl, out=rig.out)
+                                  max_seq_len=rig.msl, out=rig.out, k_scale=rig.ks, v_scale=rig.vs)
         out_h.copy_(rig.out, non_blocking=True)
 
     for _ in range(3):
@@ -817,7 +830,7 @@ def e2e_prefill(rig, steps, flush):
 def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, bf16_sus, peak_src):
     """Main line for a prefill workload: append of the new tokens + varlen
     causal prefill per step; value in TFLOP/s of visible (query, key) pairs."""
-    rig = PrefillRig(plan, dev)
+    rig = PrefillRig(plan, dev, args.kv_dtype)
     g_step = capture(rig.step, stream)
     g_pf = capture(rig.prefill, stream)
     for _ in range(args.warmup):
@@ -852,18 +865,21 @@ def run_prefill_line(args, rank, world, local, plan, dev, flush, stream, bf16, b
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "ms_per_step_median": round(max_over_ranks(statistics.median(times), world), 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV, f16 products" if rig.kv8 else "bf16",
         "data": "synthetic",
         "config": {"workload": plan.name, "batch": plan.batch, "num_q_heads": plan.num_q_heads,
                    "num_kv_heads": plan.num_kv_heads, "head_dim": plan.head_dim,
-                   "page_size": plan.page_size, "new_tokens": plan.total_new,
+                   "page_size": plan.page_size, "kv_dtype": args.kv_dtype, "new_tokens": plan.total_new,
                    "visible_pairs": wl.prefill_visible_pairs(plan), "flops_per_step": flops,
                    "step": "append new tokens + varlen causal prefill",
                    "l2": "flushed between timed steps (256 MB write + 256 MB read, untimed)",
                    "timing": "mean of the timed steps (CUDA events, one graph replay each)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
-                     "frac": round(achieved / bf16, 4), "traffic": traffic_for(f"prefill:{plan.name}"),
-                     "kernel": "paged_attention_prefill (prefill_tc_kernel)", "ms_per_launch": round(pf_ms, 5),
+                     "frac": round(achieved / bf16, 4),
+                     "traffic": traffic_for(f"prefill:{plan.name}" + (":e4m3" if rig.kv8 else "")),
+                     "kernel": "paged_attention_prefill (prefill_tc_kernel" + (", e4m3 pools)" if rig.kv8 else ")"),
+                     "ms_per_launch": round(pf_ms, 5),
                      "peak_source": peak_src + " (bf16 burst)", "peak_sustained": bf16_sus,
                      "frac_of_sustained": round(achieved / bf16_sus, 4)},
         "cpu_baseline": cpu,
@@ -996,6 +1012,20 @@ def run_extra(dev, flush, stream, hbm, bf16, bf16_sus, read_peak, steps=30):
             "append_frac_hbm": round(ab / (ams * 1e-3) / 1e9 / hbm, 4)}
     except Exception as ex:
         res["chunked_prefill"] = {"error": repr(ex)[:200]}
+    try:  # the same prefill on e4m3 pools (f16 products; codes converted in shared memory)
+        plan = wl.named_plan("chunked_prefill")
+        rig8 = PrefillRig(plan, dev, "e4m3")
+        g = capture(rig8.prefill, stream)
+        ms8 = statistics.mean(timed_graph(g, steps, flush, stream))
+        tf8 = wl.prefill_flops(plan) / (ms8 * 1e-3) / 1e12
+        ent = {"prefill_ms": round(ms8, 4), "TFLOPs": round(tf8, 1), "frac_bf16_burst": round(tf8 / bf16, 4)}
+        if "prefill_ms" in res.get("chunked_prefill", {}):
+            ent["time_vs_bf16_pool"] = round(ms8 / res["chunked_prefill"]["prefill_ms"], 3)
+        res["chunked_prefill_fp8"] = ent
+        del rig8, g
+        torch.cuda.empty_cache()
+    except Exception as ex:
+        res["chunked_prefill_fp8"] = {"error": repr(ex)[:200]}
     return res
 
 

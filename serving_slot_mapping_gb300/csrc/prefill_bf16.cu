@@ -37,8 +37,9 @@
 // Fully masked key tiles are never loaded or multiplied.
 //
 // e4m3 pools (KV8): the TMA lands each page's codes ([keys][D B], unswizzled)
-// in the upper half of the K or V ring slot, and an eleventh warp converts the
-// tile in place into the f16 layout above (cvt e4m3x2 -> f16x2 is exact:
+// in the upper half of the K or V ring slot, and two more warps (one for K,
+// one for V, so that neither ring waits on the other's conversions) convert
+// the tile in place into the f16 layout above (cvt e4m3x2 -> f16x2 is exact:
 // every e4m3 value is an f16), zeroing rows at or past L_b.  Q is staged and P
 // written as f16, so both products are kind::f16 with f16 operands; k_scale is
 // folded into the softmax scale and v_scale into the final normalisation.
@@ -60,8 +61,8 @@ constexpr int kNSK = 3;              // K ring stages
 constexpr int kNSV = 2;              // V ring stages
 constexpr int kMmaWarp = 8;          // warps 0..7: softmax of query tile (warp / 4)
 constexpr int kTmaWarp = 9;
-constexpr int kCvtWarp = 10;         // e4m3 pools: converts landed code tiles to f16
-// 10 warps (11 for e4m3 pools): at most 3 on an SM sub-partition, so at most
+constexpr int kCvtWarp = 10;         // e4m3 pools: warp 10 converts landed K tiles to f16, warp 11 V tiles
+// 10 warps (12 for e4m3 pools): at most 3 on an SM sub-partition, so at most
 // 168 registers a thread; the softmax holds half a row of S (64 fp32) at a time
 constexpr int kSlab = kBM * 128;     // one 64-column slab of a 128-row Q tile (16 KB)
 constexpr float kRescaleThreshold = 8.f;  // log2 units
@@ -69,7 +70,7 @@ constexpr int kBarSlots = 24;
 
 template <int D, bool KV8 = false>
 struct PCfg {
-  static constexpr int kThreads = 32 * (KV8 ? 11 : 10);
+  static constexpr int kThreads = 32 * (KV8 ? 12 : 10);
   static constexpr int kSlabs = D / 64;
   static constexpr int kRowBlock = kSlabs * 1024;      // one 8-key block of a K/V tile, all slabs
   static constexpr int kQBytes = kSlabs * kSlab;       // one Q tile
@@ -351,22 +352,19 @@ __global__ void __launch_bounds__(PCfg<D, KV8>::kThreads, 1)
   }
 
 
-  if (KV8 && warp == kCvtWarp) {
-    // ======================= e4m3 -> f16 converter (one warp) =======================
-    // Tiles in the order the MMA thread consumes them: K(j), V(j), K(j+1), ...
+  if (KV8 && (warp == kCvtWarp || warp == kCvtWarp + 1)) {
+    // ======================= e4m3 -> f16 converters (K: warp 10, V: warp 11) =======================
+    // Each converts its ring's tiles in order, as they land.
+    const bool isv = warp == kCvtWarp + 1;
+    const int nslots = isv ? kNSV : kNSK;
     for (int j = jb; j < nt && alive; ++j) {
-      const int jl = j - jb, valid = min(L - j * kBN, kBN);
-      const int sk = jl % kNSK, sv = jl % kNSV;
-      alive = __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL + sk), (uint32_t)((jl / kNSK) & 1), p.err));
-      convert_tile_e4m3<D>(smem + C::kKOff + sk * C::kKVTile, valid, lane);
+      const int jl = j - jb, valid = min(L - j * kBN, kBN), sl = jl % nslots;
+      alive = __all_sync(0xffffffffu,
+                         mbar_wait(bar((isv ? B_VFULL : B_KFULL) + sl), (uint32_t)((jl / nslots) & 1), p.err));
+      convert_tile_e4m3<D>(smem + (isv ? C::kVOff : C::kKOff) + sl * C::kKVTile, valid, lane);
       fence_proxy_async_smem();  // the f16 tile before the tensor core reads it
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_KREADY + sk));
-      if (alive) alive = __all_sync(0xffffffffu, mbar_wait(bar(B_VFULL + sv), (uint32_t)((jl / kNSV) & 1), p.err));
-      convert_tile_e4m3<D>(smem + C::kVOff + sv * C::kKVTile, valid, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_VREADY + sv));
+      if (lane == 0) mbar_arrive(bar((isv ? B_VREADY : B_KREADY) + sl));
     }
   }
 
