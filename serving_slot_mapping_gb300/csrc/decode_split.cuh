@@ -252,7 +252,12 @@ __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb
 template <int D, int HB, int RT, bool KV8 = false>
 struct Cfg {
   static constexpr int kConsumers = 8;
-  static constexpr int NBS = kConsumers / (HB * RT);      // blocks per stage
+  // 16-key blocks a consumer warp takes per stage: two for 32-row groups, so
+  // each of those warps (latency-bound, one per row tile) carries twice the
+  // keys through one softmax step and has independent MMA chains to overlap
+  static constexpr int BPW = RT;
+  static constexpr int NBS = kConsumers * BPW / (HB * RT);  // blocks per stage
+  static constexpr int NW = NBS / BPW;                      // consumer warps per (head, row tile)
   static constexpr int kKvProducers = 2;                  // KV producer warps, alternating stages
   static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1);  // + Q producer warp
   // bf16 pools land as 128-byte-swizzled slabs of 64 dims; e4m3 pools land a
@@ -288,7 +293,7 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   using C = Cfg<D, HB, RT, KV8>;
   Layout L;
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
-  const int merge = C::NBS > 1 ? HB * G * (D + 2) * 4 : 0;  // one slot: the chained merge below
+  const int merge = C::NW > 1 ? HB * G * (D + 2) * 4 : 0;  // one slot: the chained merge below
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
   const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 128 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
@@ -306,7 +311,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         DecodeParams p) {
   using C = Cfg<D, HB, RT, KV8>;
-  constexpr int NBS = C::NBS;
+  constexpr int NBS = C::NBS, BPW = C::BPW, NW = C::NW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -634,8 +639,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
 
   // ======================= consumer warps =======================
   const int h = warp % HB;               // head within the box
-  const int jw = (warp / HB) % NBS;      // block within each stage
-  const int rt = warp / (HB * NBS);      // row tile: query heads rt*16 .. rt*16+15 of the group
+  const int jw = (warp / HB) % NW;       // blocks jw * BPW .. jw * BPW + BPW - 1 of each stage
+  const int rt = warp / (HB * NW);       // row tile: query heads rt*16 .. rt*16+15 of the group
   const int rA = rt * 16 + (lane >> 2), rB = rA + 8;
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
@@ -682,103 +687,125 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
 
     for (int done = 0; done < seg_blocks;) {
       const int nbs = min(NBS, seg_blocks - done);
-      // fused append: this warp's block is the sequence's last, whose row
-      // L_b - 1 is the new token; fetch this lane's 8 elements of the new K / V
-      // row of head hk before the wait (lanes 0 .. D/8 - 1: K, then V)
-      const bool new_row = FUSED && jw < nbs && first_k + done + jw == cc.nblk - 1 &&
-                           __ldg(p.new_slots + cc.b) >= 0;
+      // fused append: one of this warp's blocks may be the sequence's last,
+      // whose row L_b - 1 is the new token; fetch this lane's 8 elements of
+      // the new K / V row of head hk before the wait (lanes 0 .. D/8 - 1: K,
+      // then V)
+      const int last_jb = cc.nblk - 1 - (first_k + done);  // the last block's index in this stage
+      const int new_bb = (FUSED && last_jb >= jw * BPW && last_jb < jw * BPW + BPW && last_jb < nbs &&
+                          __ldg(p.new_slots + cc.b) >= 0)
+                             ? last_jb - jw * BPW
+                             : -1;
       constexpr int kRowChunks = D / 8;  // lanes per tensor
       uint4 nr = make_uint4(0, 0, 0, 0);
-      if (new_row && lane < 2 * kRowChunks) {
+      if (new_bb >= 0 && lane < 2 * kRowChunks) {
         const int T = lane / kRowChunks, e8 = lane - T * kRowChunks;
         nr = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(T ? p.new_v : p.new_k) +
                                                   ((int64_t)cc.b * Hkv + hk) * D) + e8);
       }
       if (alive) alive = mbar_wait(full_bar(slot), phase, p.err);
-      if (jw < nbs) {
+      if (jw * BPW < nbs) {
         unsigned char* st = ring + slot * C::kStageBytes;
-        unsigned char* kt = st + (jw * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
-        unsigned char* vt = st + ((NBS + jw) * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
-        const int valid = cc.L - (first_k + done + jw) * 16;  // >= 1
-        if (valid < 16) {
-          // rows past L_b may hold stale or poisoned data (NaN would survive
-          // P = 0): zero them in V; K is masked below.  A row's chunks stay in
-          // the row under either swizzle.
-          constexpr int kCh = C::kRowBytes / 16;  // 16-byte chunks of a row of one slab
-          for (int e = lane; e < (16 - valid) * C::kSlabs * kCh; e += 32) {
-            const int row = valid + e / (C::kSlabs * kCh);
-            const int rem = e % (C::kSlabs * kCh);
-            *reinterpret_cast<uint4*>(vt + (rem / kCh) * C::kBoxBytes + row * C::kRowBytes + (rem % kCh) * 16) =
-                make_uint4(0, 0, 0, 0);
+        float s[2 * BPW][4];
+        int valid[BPW];
+        uint32_t vbase[BPW];
+        bool touched = false;  // shared-memory stores this warp made into the stage
+#pragma unroll
+        for (int bb = 0; bb < BPW; ++bb) {
+          const int jb = jw * BPW + bb;  // block within the stage
+          s[2 * bb][0] = s[2 * bb][1] = s[2 * bb][2] = s[2 * bb][3] = 0.f;
+          s[2 * bb + 1][0] = s[2 * bb + 1][1] = s[2 * bb + 1][2] = s[2 * bb + 1][3] = 0.f;
+          valid[bb] = jb < nbs ? cc.L - (first_k + done + jb) * 16 : 0;  // >= 1 for a block of the stage
+          unsigned char* kt = st + (jb * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
+          unsigned char* vt = st + ((NBS + jb) * C::kSlabs) * C::kBoxBytes + h * C::kHeadTile;
+          vbase[bb] = smem_u32(vt);
+          if (jb >= nbs) continue;
+          if (valid[bb] < 16) {
+            // rows past L_b may hold stale or poisoned data (NaN would survive
+            // P = 0): zero them in V; K is masked below.  A row's chunks stay in
+            // the row under either swizzle.
+            constexpr int kCh = C::kRowBytes / 16;  // 16-byte chunks of a row of one slab
+            for (int e = lane; e < (16 - valid[bb]) * C::kSlabs * kCh; e += 32) {
+              const int row = valid[bb] + e / (C::kSlabs * kCh);
+              const int rem = e % (C::kSlabs * kCh);
+              *reinterpret_cast<uint4*>(vt + (rem / kCh) * C::kBoxBytes + row * C::kRowBytes + (rem % kCh) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            __syncwarp();
+            touched = true;
           }
-          __syncwarp();
+          if (bb == new_bb) {
+            // the new token's K and V rows (row L_b - 1 of this block) come from
+            // the input: the pool row may still be in flight from the append above
+            const int r = valid[bb] - 1;
+            if (lane < 2 * kRowChunks) {
+              const int T = lane / kRowChunks, e8 = lane - T * kRowChunks;  // elements 8*e8 .. 8*e8 + 7
+              unsigned char* tile = T ? vt : kt;
+              if (KV8)  // 8 codes: half of 16-byte chunk e8 / 2 (a chunk stays contiguous under the swizzle)
+                *reinterpret_cast<uint2*>(tile + sw_e4m3<D>(r, e8 >> 1) + (e8 & 1) * 8) =
+                    quantize8(nr, T ? p.v_quant : p.k_quant);
+              else
+                *reinterpret_cast<uint4*>(tile + sw128(r, e8, C::kBoxBytes)) = nr;
+            }
+            __syncwarp();
+            touched = true;
+          }
+          const uint32_t kbase = smem_u32(kt);
+          if (KV8) {
+            // e4m3 K as 16-bit pairs: matrix m = keys (m & 1) * 8 .. + 7 of
+            // 16-dim chunk 2 * q2 + (m >> 1); lane gets 4 codes of key lane / 4,
+            // dims 4c .. 4c + 3: the first two are B register 0, the last two 1
+#pragma unroll
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+              uint32_t r0, r1, r2, r3;
+              ldmatrix_x4(kbase + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
+              mma_f16_16816(s[2 * bb], qf[2 * q2], e4m3x2_lo_to_f16x2(r0), e4m3x2_hi_to_f16x2(r0));
+              mma_f16_16816(s[2 * bb + 1], qf[2 * q2], e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r1));
+              mma_f16_16816(s[2 * bb], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r2), e4m3x2_hi_to_f16x2(r2));
+              mma_f16_16816(s[2 * bb + 1], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r3));
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kBoxBytes), b0, b1, b2, b3);
+              mma_bf16_16816(s[2 * bb], qf[kk], b0, b1);
+              mma_bf16_16816(s[2 * bb + 1], qf[kk], b2, b3);
+            }
+          }
         }
-        if (new_row) {
-          // the new token's K and V rows (row L_b - 1 of this block) come from
-          // the input: the pool row may still be in flight from the append above
-          const int r = valid - 1;
-          if (lane < 2 * kRowChunks) {
-            const int T = lane / kRowChunks, e8 = lane - T * kRowChunks;  // elements 8*e8 .. 8*e8 + 7
-            unsigned char* tile = T ? vt : kt;
-            if (KV8)  // 8 codes: half of 16-byte chunk e8 / 2 (a chunk stays contiguous under the swizzle)
-              *reinterpret_cast<uint2*>(tile + sw_e4m3<D>(r, e8 >> 1) + (e8 & 1) * 8) =
-                  quantize8(nr, T ? p.v_quant : p.k_quant);
-            else
-              *reinterpret_cast<uint4*>(tile + sw128(r, e8, C::kBoxBytes)) = nr;
-          }
-          __syncwarp();
-        }
-        const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-        float s[2][4];
 #pragma unroll
-        for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
-        if (KV8) {
-          // e4m3 K as 16-bit pairs: matrix m = keys (m & 1) * 8 .. + 7 of
-          // 16-dim chunk 2 * q2 + (m >> 1); lane gets 4 codes of key lane / 4,
-          // dims 4c .. 4c + 3: the first two are B register 0, the last two 1
-#pragma unroll
-          for (int q2 = 0; q2 < D / 32; ++q2) {
-            uint32_t r0, r1, r2, r3;
-            ldmatrix_x4(kbase + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
-            mma_f16_16816(s[0], qf[2 * q2], e4m3x2_lo_to_f16x2(r0), e4m3x2_hi_to_f16x2(r0));
-            mma_f16_16816(s[1], qf[2 * q2], e4m3x2_lo_to_f16x2(r1), e4m3x2_hi_to_f16x2(r1));
-            mma_f16_16816(s[0], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r2), e4m3x2_hi_to_f16x2(r2));
-            mma_f16_16816(s[1], qf[2 * q2 + 1], e4m3x2_lo_to_f16x2(r3), e4m3x2_hi_to_f16x2(r3));
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(kbase + sw128((mi >> 1) * 8 + rr, kk * 2 + (mi & 1), C::kBoxBytes), b0, b1, b2, b3);
-            mma_bf16_16816(s[0], qf[kk], b0, b1);
-            mma_bf16_16816(s[1], qf[kk], b2, b3);
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < 2 * BPW; ++t)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int key = t * 8 + (lane & 3) * 2 + (e & 1);
-            s[t][e] = key < valid ? s[t][e] * sl2 : -INFINITY;
+            const int key = (t & 1) * 8 + (lane & 3) * 2 + (e & 1);
+            s[t][e] = key < valid[t >> 1] ? s[t][e] * sl2 : -INFINITY;
           }
-        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 2 * BPW; ++t) {
+          mx0 = fmaxf(mx0, fmaxf(s[t][0], s[t][1]));
+          mx1 = fmaxf(mx1, fmaxf(s[t][2], s[t][3]));
+        }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-        float p_[2][4];
+        float p_[2 * BPW][4];
+        float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < 2 * BPW; ++t) {
           p_[t][0] = fast_exp2(s[t][0] - mn0);
           p_[t][1] = fast_exp2(s[t][1] - mn0);
           p_[t][2] = fast_exp2(s[t][2] - mn1);
           p_[t][3] = fast_exp2(s[t][3] - mn1);
+          rs0 += p_[t][0] + p_[t][1];
+          rs1 += p_[t][2] + p_[t][3];
         }
-        l0 = l0 * al0 + (p_[0][0] + p_[0][1] + p_[1][0] + p_[1][1]);
-        l1 = l1 * al1 + (p_[0][2] + p_[0][3] + p_[1][2] + p_[1][3]);
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
         if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
           for (int n8 = 0; n8 < D / 8; ++n8) {
@@ -788,46 +815,51 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         }
         m0 = mn0;
         m1 = mn1;
-        uint32_t pa[4];
-        if (KV8) {
-          pa[0] = pack_f16(p_[0][0], p_[0][1]);
-          pa[1] = pack_f16(p_[0][2], p_[0][3]);
-          pa[2] = pack_f16(p_[1][0], p_[1][1]);
-          pa[3] = pack_f16(p_[1][2], p_[1][3]);
-        } else {
-          pa[0] = pack_bf16(p_[0][0], p_[0][1]);
-          pa[1] = pack_bf16(p_[0][2], p_[0][3]);
-          pa[2] = pack_bf16(p_[1][0], p_[1][1]);
-          pa[3] = pack_bf16(p_[1][2], p_[1][3]);
-        }
-        if (KV8) {
-          // e4m3 V, transposed as 16-bit pairs: lane gets keys 2c, 2c + 1 of
-          // dims 2j, 2j + 1 (j = lane / 4) of a 16-dim chunk, regrouped to key
-          // pairs per dim; the even dims form output tile 2 * chunk, the odd
-          // ones tile 2 * chunk + 1, so o[t] column n is dim (t / 2) * 16 + 2n + t % 2
 #pragma unroll
-          for (int q2 = 0; q2 < D / 32; ++q2) {
-            uint32_t r0, r1, r2, r3;
-            ldmatrix_x4_trans(vbase + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
-            r0 = __byte_perm(r0, 0u, 0x3120);  // (key 2c, key 2c+1) of dim 2j | same of dim 2j+1
-            r1 = __byte_perm(r1, 0u, 0x3120);
-            r2 = __byte_perm(r2, 0u, 0x3120);
-            r3 = __byte_perm(r3, 0u, 0x3120);
-            mma_f16_16816(o[4 * q2], pa, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1));
-            mma_f16_16816(o[4 * q2 + 1], pa, e4m3x2_hi_to_f16x2(r0), e4m3x2_hi_to_f16x2(r1));
-            mma_f16_16816(o[4 * q2 + 2], pa, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3));
-            mma_f16_16816(o[4 * q2 + 3], pa, e4m3x2_hi_to_f16x2(r2), e4m3x2_hi_to_f16x2(r3));
+        for (int bb = 0; bb < BPW; ++bb) {
+          if (jw * BPW + bb >= nbs) continue;
+          uint32_t pa[4];
+          if (KV8) {
+            pa[0] = pack_f16(p_[2 * bb][0], p_[2 * bb][1]);
+            pa[1] = pack_f16(p_[2 * bb][2], p_[2 * bb][3]);
+            pa[2] = pack_f16(p_[2 * bb + 1][0], p_[2 * bb + 1][1]);
+            pa[3] = pack_f16(p_[2 * bb + 1][2], p_[2 * bb + 1][3]);
+          } else {
+            pa[0] = pack_bf16(p_[2 * bb][0], p_[2 * bb][1]);
+            pa[1] = pack_bf16(p_[2 * bb][2], p_[2 * bb][3]);
+            pa[2] = pack_bf16(p_[2 * bb + 1][0], p_[2 * bb + 1][1]);
+            pa[3] = pack_bf16(p_[2 * bb + 1][2], p_[2 * bb + 1][3]);
           }
-        } else {
+          if (KV8) {
+            // e4m3 V, transposed as 16-bit pairs: lane gets keys 2c, 2c + 1 of
+            // dims 2j, 2j + 1 (j = lane / 4) of a 16-dim chunk, regrouped to key
+            // pairs per dim; the even dims form output tile 2 * chunk, the odd
+            // ones tile 2 * chunk + 1, so o[t] column n is dim (t / 2) * 16 + 2n + t % 2
 #pragma unroll
-          for (int jj = 0; jj < D / 16; ++jj) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(vbase + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kBoxBytes), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * jj], pa, b0, b1);
-            mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+              uint32_t r0, r1, r2, r3;
+              ldmatrix_x4_trans(vbase[bb] + sw_e4m3<D>((mi & 1) * 8 + rr, 2 * q2 + (mi >> 1)), r0, r1, r2, r3);
+              r0 = __byte_perm(r0, 0u, 0x3120);  // (key 2c, key 2c+1) of dim 2j | same of dim 2j+1
+              r1 = __byte_perm(r1, 0u, 0x3120);
+              r2 = __byte_perm(r2, 0u, 0x3120);
+              r3 = __byte_perm(r3, 0u, 0x3120);
+              mma_f16_16816(o[4 * q2], pa, e4m3x2_lo_to_f16x2(r0), e4m3x2_lo_to_f16x2(r1));
+              mma_f16_16816(o[4 * q2 + 1], pa, e4m3x2_hi_to_f16x2(r0), e4m3x2_hi_to_f16x2(r1));
+              mma_f16_16816(o[4 * q2 + 2], pa, e4m3x2_lo_to_f16x2(r2), e4m3x2_lo_to_f16x2(r3));
+              mma_f16_16816(o[4 * q2 + 3], pa, e4m3x2_hi_to_f16x2(r2), e4m3x2_hi_to_f16x2(r3));
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < D / 16; ++jj) {
+              uint32_t b0, b1, b2, b3;
+              ldmatrix_x4_trans(vbase[bb] + sw128((mi & 1) * 8 + rr, 2 * jj + (mi >> 1), C::kBoxBytes), b0, b1, b2,
+                                b3);
+              mma_bf16_16816(o[2 * jj], pa, b0, b1);
+              mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+            }
           }
         }
-        if (valid < 16 || new_row) fence_proxy_async_smem();  // our stores precede the next TMA into this slot
+        if (touched) fence_proxy_async_smem();  // our stores precede the next TMA into this slot
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
@@ -862,11 +894,11 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     const int64_t seg_id = (int64_t)cc.b * Hg + cc.hk;
     const int64_t pslot = (seg_id + c) * HB + h;  // unique per (segment, CTA, head)
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(p.out) + ((int64_t)cc.b * Hq + (int64_t)hk * G) * D;
-    if (NBS > 1) {
-      // NBS warps share each head and row tile, each with the state of its
-      // block of every stage: chained through one shared-memory slot, warp
-      // NBS - 1 hands its state to warp NBS - 2, ... down to warp 0 (one slot
-      // instead of NBS leaves room for another stage of the ring).
+    if (NW > 1) {
+      // NW warps share each head and row tile, each with the state of its
+      // blocks of every stage: chained through one shared-memory slot, warp
+      // NW - 1 hands its state to warp NW - 2, ... down to warp 0 (one slot
+      // instead of NW leaves room for another stage of the ring).
       // o_w = 2^(m_w - M) o_w + 2^(m_x - M) o_x, the same for l, M = max(m_w, m_x).
       float* mo = mrg_o + (h * G) * D;
       float* mml = mrg_ml + (h * G) * 2;
@@ -881,7 +913,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
         }
       };
 #pragma unroll 1
-      for (int w = NBS - 1; w >= 1; --w) {
+      for (int w = NW - 1; w >= 1; --w) {
         if (jw == w) {
           if ((lane & 3) == 0) {
             if (rA < G) { mml[rA * 2] = m0; mml[rA * 2 + 1] = la; }
