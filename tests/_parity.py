@@ -15,10 +15,13 @@ F32_MAX_ABS = 1e-5
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """Raw element bits (uint16 for bf16, float32 array for f32) on the host."""
+    """Raw element bits (uint16 for bf16, uint8 codes for e4m3, float32 array
+    for f32) on the host."""
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 
@@ -94,8 +97,9 @@ def compact_subset(st: wl.StepTensors, seqs):
     uniq = sorted(set(pages))
     remap = {p: i for i, p in enumerate(uniq)}
     idx = torch.tensor(uniq, dtype=torch.long, device=st.key_pool.device)
-    kp = bits(st.key_pool.index_select(0, idx))
-    vp = bits(st.value_pool.index_select(0, idx))
+    raw = lambda t: t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t  # e4m3: select the code bytes
+    kp = bits(raw(st.key_pool).index_select(0, idx))
+    vp = bits(raw(st.value_pool).index_select(0, idx))
     mb = plan.block_table.shape[1]
     bt = np.full((len(seqs), mb), -1, dtype=np.int64)
     slots = []

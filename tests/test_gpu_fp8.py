@@ -166,3 +166,41 @@ def test_fp8_prefill_csr_matches_row_padded(cuda_device):
                                             k_scale=KS, v_scale=VS)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_fp8_long_context_full_every_sequence(cuda_device):
+    """The long-context GQA workload at full size (256 sequences, contexts
+    U[1024, 32768]) on e4m3 pools.  The cached tokens' codes are made on the
+    device by torch's own e4m3 conversion (x / scale, the oracle's rule for
+    these in-range values); the appended rows go through the library's
+    quantising append, checked byte for byte against the oracle's quantiser;
+    then every sequence's decode output against the oracle on the codes, 16
+    sequences at a time on host copies of only the pages they read."""
+    from _parity import compact_subset
+    plan = wl.long_context_plan(hkv=8, seed=4)
+    st = wl.materialize(plan, cuda_device)
+    for name in ("key_pool", "value_pool"):  # bf16 pool -> codes, in slices of pages
+        src = getattr(st, name)
+        dst = torch.empty(src.shape, dtype=torch.float8_e4m3fn, device=cuda_device)
+        for i in range(0, src.shape[0], 4096):
+            dst[i:i + 4096] = (src[i:i + 4096].float() / KS).to(torch.float8_e4m3fn)
+        setattr(st, name, dst)
+        del src
+    torch.cuda.empty_cache()
+    capi.paged_kv_append(st.key_pool, st.value_pool, st.key, st.value, st.slot_mapping, k_scale=KS, v_scale=KS)
+    out = capi.paged_attention_decode(st.key_pool, st.value_pool, st.q, st.block_table, st.seq_lens, plan.scale,
+                                      max_seq_len=int(plan.seq_lens.max()), k_scale=KS, v_scale=KS)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    P, ps = plan.num_pages, plan.page_size
+    got_rows = st.key_pool.view(torch.uint8).view(P * ps, -1)[st.slot_mapping].cpu().numpy()
+    exp_rows = kv_fp8.quantize(to_f64(bits(st.key)).astype(np.float32), KS).reshape(len(plan.slot_mapping), -1)
+    assert np.array_equal(got_rows, exp_rows)              # the appended codes
+    q_all = to_f64(bits(st.q))
+    exp = np.zeros_like(q_all)
+    for s0 in range(0, plan.batch, 16):
+        seqs = list(range(s0, min(s0 + 16, plan.batch)))
+        kc, vc, btc, _, _ = compact_subset(st, seqs)       # codes after the append, as uint8
+        exp[seqs] = kv_fp8.paged_attention_decode_fp8(kc, vc, KS, KS, q_all[seqs], btc, plan.seq_lens[seqs],
+                                                      plan.scale)
+    assert_close(out, exp, "bf16", "fp8 long GQA, every sequence")
