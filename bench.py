@@ -405,7 +405,7 @@ class DecodeRig:
             self.decode_with(t)
 
     def launches_per_step(self):
-        return {"fused": 1}.get(self.mode, 2)  # append + the attention call (cascade: one launch)
+        return {"fused": 1, "cascade": 4}.get(self.mode, 2)  # cascade: append, prefix pass, split, combine
 
     # the device-resident forms
     def append(self):

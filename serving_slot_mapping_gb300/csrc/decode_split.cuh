@@ -112,6 +112,18 @@ __device__ __forceinline__ unsigned arrive_part(unsigned long long* cnt, unsigne
   return 0xFFFFFFFFu;
 }
 
+// Acquire-release fence at GPU scope (lighter than the sequentially
+// consistent fence of __threadfence; release and acquire patterns need no more).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
+
+// Load with acquire semantics at GPU scope: later reads of this thread (and,
+// through a barrier, of its CTA) see what was published before the value.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* ptr) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 // One warp merges query row (head h of the box, row g) of segment `seg`, cut
 // into parts by CTAs c0 .. c0 + nparts - 1 (a CTA that owns no unit, only
 // possible when U < n, wrote nothing and weighs 0), and writes the bf16
@@ -187,7 +199,7 @@ __device__ __noinline__ void merge_segment_row(const DecodeParams& p, int64_t se
 template <int D>
 __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb, int c0, int span, int HB, int Hg,
                                            int64_t U, int n, int row_lo, int row_hi, unsigned char* scratch,
-                                           int scratch_bytes, int tid, int nthreads) {
+                                           int scratch_bytes, int tid, int nthreads, int bar_id) {
   const int G = p.group;
   const int all_rows = HB * G;  // a part's rows (h, g), contiguous
   const int rows = row_hi - row_lo;  // the rows merged here
@@ -225,7 +237,7 @@ __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb
   }
   cp_async_commit();
   cp_async_wait<0>();
-  named_barrier(2, nthreads);
+  named_barrier(bar_id, nthreads);
   for (int x = tid; x < rows * (D / 4); x += nthreads) {
     const int r = x / (D / 4), c4 = x - r * (D / 4);
     float M = -INFINITY;
@@ -1003,7 +1015,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
             if (x < c) mine += part;
           }
         }
-        __threadfence();
+        fence_acq_rel_gpu();  // release: the partials above, then the count
         const bool last = arrive_part(p.seg_count + seg_id, *tag_slot, p.err) == (unsigned)(arrivals - 1);
         if (p.slice_merge || last) {
           const int e = pending[0];  // a CTA range cuts at most 2 segments
@@ -1023,20 +1035,31 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   if (p.pre_chunks == 0) {
     named_barrier(2, C::kConsumers * 32);  // every count of this CTA recorded; the ring is idle
     const int npend = pending[0];
-    for (int e = 0; e < npend; ++e) {
+    // A range cuts at most two segments, its first and its last.  With two to
+    // merge, the consumer warps split in halves that wait for and merge one
+    // segment each at the same time (each with half the idle ring as scratch
+    // and its own named barrier), so the later merge does not queue behind
+    // the earlier one.
+    const int groups = npend == 2 ? 2 : 1;
+    const int gsize = C::kConsumers * 32 / groups;
+    const int grp = tid / gsize, gtid = tid - grp * gsize;
+    const int bar_id = groups == 2 ? 3 + grp : 2;
+    const int scratch_bytes = S * C::kStageBytes / groups;
+    for (int e = grp; e < npend; e += groups) {
       volatile int* ent = pending + 1 + kPend * e;
       const int b = ent[0], hkb = ent[1], c0 = ent[2], span = ent[3], parts = ent[4], mine = ent[5];
-      if (p.slice_merge) {
-        // wait for the segment's last part (its CTAs are all resident and run
-        // to their range ends without waiting on anyone), then merge rows
-        // [mine, mine + 1) * rows / parts
-        if (tid == 0) {
+      if (gtid == 0) {
+        if (p.slice_merge) {
+          // wait for the segment's last part (its CTAs are all resident and
+          // run to their range ends without waiting on anyone); the acquire
+          // load that sees the full count orders the parts' partials (each
+          // published by a fence and a count) before this group's reads
           const unsigned long long tag = *tag_slot;
           const unsigned long long* cnt = p.seg_count + (int64_t)b * Hg + hkb;
           const unsigned long long limit = p.part_wait_ns != 0 ? p.part_wait_ns : kWaitLimitNs;
           const unsigned long long t0 = global_ns();
           for (;;) {
-            const unsigned long long w = *reinterpret_cast<const volatile unsigned long long*>(cnt);
+            const unsigned long long w = ld_acquire_gpu(cnt);
             if ((w >> 16) == tag && (int)(w & 0xFFFFu) >= parts) break;
             if (global_ns() - t0 > limit) {
               record_error(p.err, ERR_TIMEOUT, -2);
@@ -1044,14 +1067,16 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
             }
             __nanosleep(128);
           }
+        } else {
+          fence_acq_rel_gpu();  // this CTA counted the last part: the others' partials before its reads
         }
       }
-      if (tid == 0) __threadfence();  // the other parts' partials before this CTA's merge reads them
-      named_barrier(2, C::kConsumers * 32);
+      named_barrier(bar_id, gsize);
+      // merge rows [mine, mine + 1) * rows / parts of the segment
       const int rows = HB * p.group;
-      merge_segment<D>(p, b, hkb, c0, span, HB, Hg, U, n, mine * rows / parts, (mine + 1) * rows / parts, ring,
-                       S * C::kStageBytes, tid, C::kConsumers * 32);
-      named_barrier(2, C::kConsumers * 32);  // before the next merge reuses the ring
+      merge_segment<D>(p, b, hkb, c0, span, HB, Hg, U, n, mine * rows / parts, (mine + 1) * rows / parts,
+                       ring + grp * scratch_bytes, scratch_bytes, gtid, gsize, bar_id);
+      named_barrier(bar_id, gsize);  // before a next merge reuses the scratch
     }
   }
 }
