@@ -1,5 +1,6 @@
 // C ABI of libpagedattn.so (declared in include/paged_attn.h): host-side
 // argument checks, launch-shape choices and dispatch to the kernels.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -272,6 +273,10 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   p->kv8 = kv8(pool) ? 1 : 0;
   p->scale_log2 = (float)((double)scale * (kv8(pool) ? (double)pool->k_scale : 1.0) * kLog2e);
   p->v_scale = kv8(pool) ? pool->v_scale : 1.f;
+  // segment changes weigh in the cut (32-row groups); positions are counted in 32 bits
+  const int pen = pa::decode_segment_penalty(pool->head_dim, hb, group, kv8(pool));
+  const int64_t max_keys = std::max<int64_t>(max_seq_len, (int64_t)t.max_blocks * pool->page_size);
+  p->seg_penalty = (int64_t)batch * ((max_keys + 15) / 16 + pen) <= INT32_MAX ? pen : 0;
   p->err = error_word();
   return PA_OK;
 }
@@ -592,6 +597,7 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
   p.pre_o = pre_o;
   p.pre_ml = pre_ml;
   p.pre_chunks = chunks;
+  p.seg_penalty = 0;  // the combine kernel recomputes the plain cut of the units
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   SideStream* side = side_stream();
   if (side == nullptr) return PA_ERR_CUDA;

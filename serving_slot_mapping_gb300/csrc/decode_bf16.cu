@@ -140,6 +140,20 @@ int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size)
   return hb;
 }
 
+// 32-row groups (two row tiles): a CTA loses ~5 us at each segment change of
+// its range (measured on GB300 with per-CTA global-timer stamps: the NW
+// consumer warps' chained merge, the part's write and count, the next
+// segment's query rows).  In 16-key blocks of one head box that is the
+// change's time over one block's: its K and V bytes at ~46 GB/s (an SM's share
+// of HBM) or its MMA work at ~0.35 ns per query-key pair, whichever is longer.
+// Other shapes cut the units plainly (0).
+int decode_segment_penalty(int32_t head_dim, int32_t heads_per_box, int32_t group, bool kv8) {
+  if (group <= 16) return 0;
+  const double bytes_ns = 2.0 * 16 * heads_per_box * head_dim * (kv8 ? 1 : 2) / 46.0;
+  const double mma_ns = 16.0 * heads_per_box * group * 0.35;
+  return (int)(5000.0 / (bytes_ns > mma_ns ? bytes_ns : mma_ns) + 0.5);
+}
+
 int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box) {
   // (segment + CTA) * HB + head over segments (b, head box): B*Hkv + n*HB at most
   return (int64_t)batch * num_kv_heads + (int64_t)num_ctas * heads_per_box;

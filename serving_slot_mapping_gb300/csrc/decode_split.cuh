@@ -71,7 +71,8 @@ __device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b, int max_
   return seq_keys(p.seq_lens, p.kv_indptr, p.kv_last_page_len, p.kv_len, b, p.pool.page_size, max_len, nullptr);
 }
 
-// CTA that owns unit u when U units are cut into n ranges [c*U/n, (c+1)*U/n).
+// CTA that owns unit u when U units are cut into n ranges [c*U/n, (c+1)*U/n)
+// (the same for a position of the weighted cut below, with W positions).
 __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int n) {
   return (int)(((u + 1) * (int64_t)n - 1) / U);
 }
@@ -271,7 +272,14 @@ struct Cfg {
   static constexpr int NBS = kConsumers * BPW / (HB * RT);  // blocks per stage
   static constexpr int NW = NBS / BPW;                      // consumer warps per (head, row tile)
   static constexpr int kKvProducers = 2;                  // KV producer warps, alternating stages
-  static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1);  // + Q producer warp
+  // 32-row groups: a segment change costs a CTA ~5 us (the NW warps' chained
+  // merge, the part's write and count), so the cut of the units weighs
+  // segment changes (seg_penalty) and a publisher warp does each cut
+  // segment's fence and count off the consumer path
+  static constexpr bool kCostlyChange = RT == 2;
+  // + the Q producer warp (+ the publisher warp)
+  static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1 + (kCostlyChange ? 1 : 0));
+  static constexpr int kBars = kCostlyChange ? 7 : 4;  // mbarriers after the ring's two per stage
   // bf16 pools land as 128-byte-swizzled slabs of 64 dims; e4m3 pools land a
   // whole row of D codes per slot, swizzled over its D bytes (see sw_e4m3)
   static constexpr int kSlabs = KV8 ? 1 : D / 64;          // TMA slabs per row
@@ -307,12 +315,12 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NW > 1 ? HB * G * (D + 2) * 4 : 0;  // one slot: the chained merge below
   const int prefix = ((B + 1) * 4 + 127) / 128 * 128;
-  const int fixed = 2 * L.qslot + (2 * kMaxStages + 4) * 8 + 128 + merge + prefix + 128 + 1024;
+  const int fixed = 2 * L.qslot + (2 * kMaxStages + C::kBars) * 8 + 128 + merge + prefix + 128 + 1024;
   int s = (budget - fixed) / C::kStageBytes;
   if (s > kMaxStages) s = kMaxStages;
   L.stages = s;
   L.bar_off = s * C::kStageBytes + 2 * L.qslot;
-  L.mrg_off = L.bar_off + (2 * s + 4) * 8 + 128;  // + the pending-merge list
+  L.mrg_off = L.bar_off + (2 * s + C::kBars) * 8 + 128;  // + the pending-merge list
   L.prefix_off = L.mrg_off + merge;
   L.total = L.prefix_off + prefix + 1024;
   return L;
@@ -341,6 +349,11 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto qfull_bar = [&](int s) { return bars + 8u * (2 * S + s); };
   auto qempty_bar = [&](int s) { return bars + 8u * (2 * S + 2 + s); };
+  // (kCostlyChange) cut segment e (0, 1) of this range: its partial is
+  // written (consumers -> publisher); every cut segment is published
+  // (publisher -> consumers)
+  auto pub_bar = [&](int e) { return bars + 8u * (2 * S + 4 + e); };
+  const uint32_t pubd_bar = bars + 8u * (2 * S + 6);
   float* mrg_o = reinterpret_cast<float*>(smem + lay.mrg_off);       // [HB][G][D]
   float* mrg_ml = mrg_o + HB * G * D;                                 // [HB][G][2]
   int* prefix = reinterpret_cast<int*>(smem + lay.prefix_off);        // [B+1] 16-key blocks before b
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   // kPend ints each (b, head box, c0, span, parts, this CTA's part index);
   // bytes 96..103 hold this launch's counter tag
   constexpr int kPend = 6;
-  volatile int* pending = reinterpret_cast<volatile int*>(smem + lay.bar_off + (2 * S + 4) * 8);  // [24]
+  volatile int* pending = reinterpret_cast<volatile int*>(smem + lay.bar_off + (2 * S + C::kBars) * 8);  // [24]
   volatile unsigned long long* tag_slot = reinterpret_cast<volatile unsigned long long*>(pending + 24);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -365,32 +378,56 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       mbar_init(qfull_bar(s), 1);
       mbar_init(qempty_bar(s), C::kConsumers);
     }
+    if constexpr (C::kCostlyChange) {
+      mbar_init(pub_bar(0), 1);
+      mbar_init(pub_bar(1), 1);
+      mbar_init(pubd_bar, 1);
+    }
     fence_mbar_init();
   }
-  for (int b = tid; b < B; b += C::kThreads) prefix[b + 1] = nblk_of(p, b, max_len);
-  if (tid == 0) prefix[0] = 0;
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < B; base += 32) {
-      const int idx = base + lane;
-      int v = idx < B ? prefix[idx + 1] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t;
-      }
-      if (idx < B) prefix[idx + 1] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  __syncthreads();
-
-  // units: (b, head box hg, 16-key block k), sequence-major
-  const int64_t NB = prefix[B];
-  const int64_t U = NB * Hg;
   const int n = p.num_ctas, c = blockIdx.x;
-  const int64_t u0 = (int64_t)c * U / n, u1 = (int64_t)(c + 1) * U / n;
+  // Units: (b, head box hg, 16-key block k), sequence-major, cut into one
+  // range per CTA.  Plainly, the U units in n equal ranges.  With
+  // kCostlyChange they are laid out on a line of positions on which each
+  // segment (sequence x head box with keys) takes P header positions and then
+  // one per block (P = seg_penalty: a segment change's time in blocks), the W
+  // positions are cut into n equal ranges and a CTA takes the units whose
+  // positions fall in its range, so CTAs whose ranges hold more segment
+  // changes get fewer blocks.  Every range is kept longer than a header (else
+  // P = 0), so with P > 0 every CTA owns a unit.  prefix[b] counts the
+  // positions (blocks, plus P per segment) before sequence b.
+  int P = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    if constexpr (C::kCostlyChange) {
+      if (pass == 0) P = p.seg_penalty;
+      else __syncthreads();  // every thread has read the first pass's total
+    }
+    for (int b = tid; b < B; b += C::kThreads) {
+      const int nb = nblk_of(p, b, max_len);
+      prefix[b + 1] = C::kCostlyChange && nb > 0 ? nb + P : nb;
+    }
+    if (tid == 0) prefix[0] = 0;
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < B; base += 32) {
+        const int idx = base + lane;
+        int v = idx < B ? prefix[idx + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (idx < B) prefix[idx + 1] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+    __syncthreads();
+    if (!C::kCostlyChange || P == 0 || (int64_t)prefix[B] * Hg >= (int64_t)n * (P + 1)) break;
+    P = 0;
+  }
+  const int64_t W = (int64_t)prefix[B] * Hg;  // positions (units when P = 0)
+  const int64_t u0 = (int64_t)c * W / n, u1 = (int64_t)(c + 1) * W / n;
   griddep_launch_dependents();
   // Counter tag of this launch, kept by thread 0 (the only thread that counts
   // arrivals) in shared memory: read the epoch E, then count this CTA on the grid counter; the
@@ -457,6 +494,8 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   }
   if (u0 >= u1) return;
 
+  // the first unit at position u or after it (u in a header: the segment's
+  // first unit); cur.u is the unit's position
   auto locate = [&](int64_t u) {
     Cursor cur;
     const int x = (int)(u / Hg);
@@ -466,12 +505,21 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       if (prefix[mid] <= x) lo = mid; else hi = mid;
     }
     cur.b = lo;
-    cur.nblk = prefix[lo + 1] - prefix[lo];
     const int r = (int)(u - (int64_t)Hg * prefix[lo]);
-    cur.hk = r / cur.nblk;  // head box index
-    cur.k = r - cur.hk * cur.nblk;
+    if constexpr (C::kCostlyChange) {
+      const int seg = prefix[lo + 1] - prefix[lo];  // positions of one head box's segment
+      cur.nblk = seg - P;
+      cur.hk = r / seg;
+      const int off = r - cur.hk * seg;
+      cur.k = off >= P ? off - P : 0;
+      cur.u = (int64_t)Hg * prefix[lo] + (int64_t)cur.hk * seg + P + cur.k;
+    } else {
+      cur.nblk = prefix[lo + 1] - prefix[lo];
+      cur.hk = r / cur.nblk;  // head box index
+      cur.k = r - cur.hk * cur.nblk;
+      cur.u = u;
+    }
     cur.L = seq_len_of(p, cur.b, max_len);
-    cur.u = u;
     return cur;
   };
   auto advance = [&](Cursor& cur, int nb) {
@@ -479,11 +527,12 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     cur.k += nb;
     if (cur.k == cur.nblk) {
       cur.k = 0;
+      if constexpr (C::kCostlyChange) cur.u += P;  // the next segment's header
       if (++cur.hk == Hg) {
         cur.hk = 0;
         do { ++cur.b; } while (cur.b < B && prefix[cur.b + 1] == prefix[cur.b]);
         if (cur.b < B) {
-          cur.nblk = prefix[cur.b + 1] - prefix[cur.b];
+          cur.nblk = prefix[cur.b + 1] - prefix[cur.b] - (C::kCostlyChange ? P : 0);
           cur.L = seq_len_of(p, cur.b, max_len);
         }
       }
@@ -517,6 +566,61 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       advance(cur, (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u));
     }
     return;
+  }
+
+  if constexpr (C::kCostlyChange) {
+    if (warp == C::kConsumers + C::kKvProducers + 1) {
+      // ======================= part publisher =======================
+      // For each segment of this range cut across CTAs (plain decode: a range
+      // cuts at most two, its first and its last), wait until the consumers
+      // have written this CTA's partial of it, then publish it: a GPU-scope
+      // release fence (cumulative over the consumers' writes, which the
+      // mbarrier's release/acquire orders before it) and a count on the
+      // segment's counter; note the merge this CTA then takes part in.  Done
+      // here, the fence's wait for the partial writes and the counter's round
+      // trip hold up no consumer warp, so no stage of the ring is freed late.
+      if (lane != 0) return;
+      if (p.pre_chunks == 0) {
+        Cursor cur = locate(u0);
+        bool alive = true;
+        for (int e = 0; cur.u < u1;) {
+          const int seg_blocks = (int)min((int64_t)(cur.nblk - cur.k), u1 - cur.u);
+          if (!(cur.k == 0 && seg_blocks == cur.nblk)) {
+            if (alive) alive = mbar_wait(pub_bar(e), 0, p.err);
+            const int64_t seg_id = (int64_t)cur.b * Hg + cur.hk;
+            // positions of the segment's first and last units
+            const int64_t us = (int64_t)Hg * prefix[cur.b] + (int64_t)cur.hk * (cur.nblk + P) + P;
+            const int c0 = cta_of_unit(us, W, n), c1 = cta_of_unit(us + cur.nblk - 1, W, n);
+            int arrivals = c1 - c0 + 1, mine = c - c0;  // CTAs c0 .. c1 own the segment's units ...
+            if (W < n) {  // ... except those without a unit, which took no part (only when P = 0)
+              arrivals = mine = 0;
+              for (int x = c0; x <= c1; ++x) {
+                const int part = cta_range_empty(x, W, n) ? 0 : 1;
+                arrivals += part;
+                if (x < c) mine += part;
+              }
+            }
+            fence_acq_rel_gpu();  // release: the partials, then the count
+            const bool last = arrive_part(p.seg_count + seg_id, *tag_slot, p.err) == (unsigned)(arrivals - 1);
+            if (p.slice_merge || last) {
+              const int pe = pending[0];
+              volatile int* ent = pending + 1 + kPend * pe;
+              ent[0] = cur.b;
+              ent[1] = cur.hk;
+              ent[2] = c0;
+              ent[3] = c1 - c0 + 1;  // the merge walks the CTA span (empty CTAs weigh 0)
+              ent[4] = p.slice_merge ? arrivals + p.test_extra_parts : 1;
+              ent[5] = p.slice_merge ? mine : 0;
+              pending[0] = pe + 1;
+            }
+            ++e;
+          }
+          advance(cur, seg_blocks);
+        }
+      }
+      mbar_arrive(pubd_bar);
+      return;
+    }
   }
 
   if (warp >= C::kConsumers && warp < C::kConsumers + C::kKvProducers) {
@@ -657,6 +761,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   const float sl2 = p.scale_log2;
   const int mi = lane >> 3, rr = lane & 7;
   Cursor cc = locate(u0);
+  int ncut = 0;        // (kCostlyChange) cut segments handed to the publisher so far
   int slot = 0;        // ring slot of the next stage (stage index % S)
   uint32_t phase = 0;  // its full-barrier parity ((stage index / S) & 1)
   bool alive = true;
@@ -998,19 +1103,24 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     if (!complete && p.pre_chunks == 0) {
       // This CTA's part of a segment cut across CTAs is written.  Publish and
       // count it: the consumer barrier orders every consumer thread's partial
-      // writes before thread 0's fence (cumulative) and count.  The segment is
-      // merged after the CTAs' ranges, with the stage rings idle: by each CTA
-      // holding a part, a slice of the rows each (co-resident grid), or else by
-      // the CTA that counts the last part.  No consumer waits here.
+      // writes before the publishing thread's fence (cumulative) and count
+      // (thread 0, or the publisher warp after thread 0's CTA-scope release on
+      // an mbarrier).  The segment is merged after the CTAs' ranges, with the
+      // stage rings idle: by each CTA holding a part, a slice of the rows each
+      // (co-resident grid), or else by the CTA that counts the last part.  No
+      // consumer waits here.
       named_barrier(2, C::kConsumers * 32);
-      if (tid == 0) {
+      if constexpr (C::kCostlyChange) {
+        if (tid == 0) mbar_arrive(pub_bar(ncut));
+        ++ncut;
+      } else if (tid == 0) {
         const int64_t us = (int64_t)Hg * prefix[cc.b] + (int64_t)cc.hk * cc.nblk;
-        const int c0 = cta_of_unit(us, U, n), c1 = cta_of_unit(us + cc.nblk - 1, U, n);
+        const int c0 = cta_of_unit(us, W, n), c1 = cta_of_unit(us + cc.nblk - 1, W, n);
         int arrivals = c1 - c0 + 1, mine = c - c0;  // CTAs c0 .. c1 own the segment's units ...
-        if (U < n) {  // ... except those without a unit, which took no part
+        if (W < n) {  // ... except those without a unit, which took no part
           arrivals = mine = 0;
           for (int x = c0; x <= c1; ++x) {
-            const int part = cta_range_empty(x, U, n) ? 0 : 1;
+            const int part = cta_range_empty(x, W, n) ? 0 : 1;
             arrivals += part;
             if (x < c) mine += part;
           }
@@ -1033,6 +1143,9 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
     advance(cc, seg_blocks);
   }
   if (p.pre_chunks == 0) {
+    if constexpr (C::kCostlyChange) {
+      if (tid == 0 && alive) alive = mbar_wait(pubd_bar, 0, p.err);  // every part of this CTA published
+    }
     named_barrier(2, C::kConsumers * 32);  // every count of this CTA recorded; the ring is idle
     const int npend = pending[0];
     // A range cuts at most two segments, its first and its last.  With two to
@@ -1074,7 +1187,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
       named_barrier(bar_id, gsize);
       // merge rows [mine, mine + 1) * rows / parts of the segment
       const int rows = HB * p.group;
-      merge_segment<D>(p, b, hkb, c0, span, HB, Hg, U, n, mine * rows / parts, (mine + 1) * rows / parts,
+      merge_segment<D>(p, b, hkb, c0, span, HB, Hg, W, n, mine * rows / parts, (mine + 1) * rows / parts,
                        ring + grp * scratch_bytes, scratch_bytes, gtid, gsize, bar_id);
       named_barrier(bar_id, gsize);  // before a next merge reuses the scratch
     }

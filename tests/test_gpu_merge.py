@@ -86,6 +86,27 @@ def test_merge_with_uninitialised_workspace(cuda_device, fill):
     assert_close(out, _expect(st, kp, vp, st.q), "bf16", f"merge, workspace {fill}")
 
 
+def _mqa_plan(seed):
+    # 32 query heads on 1 KV head (two 16-row tiles: the warps chain their
+    # states, segment changes weigh in the cut and a publisher warp counts
+    # the parts); ~190 blocks a sequence over 152 CTAs: every segment is cut
+    return wl.plan_from_lengths(f"mqa_merge_{seed}", "decode", "bf16", 32, 1, 128, 16,
+                                np.full(32, 3000) + np.arange(32) * 7, np.ones(32), seed=seed)
+
+
+def test_merge_32_row_groups_uninitialised_workspace(cuda_device):
+    plan = _mqa_plan(31)
+    st, kp, vp = _appended(plan, cuda_device)
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+    ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, generator=torch.Generator().manual_seed(8)))
+    for rep in range(2):
+        q = _new_q(st.q, 300 + rep)
+        out = _decode(st, kp, vp, q, ws)
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        assert_close(out, _expect(st, kp, vp, q), "bf16", f"32-row merge rep {rep}")
+
+
 def test_merge_repeated_calls_and_shapes_share_one_workspace(cuda_device):
     big = wl.gqa_decode_plan()
     small = wl.gqa_decode_plan(batch=5, lo=300, hi=6000, seed=9)
@@ -104,8 +125,9 @@ def test_merge_repeated_calls_and_shapes_share_one_workspace(cuda_device):
             assert_close(out, _expect(st, kp, vp, q), "bf16", f"merge rep {rep} plan {i}")
 
 
-def test_merge_in_cuda_graph_replays(cuda_device):
-    plan = wl.gqa_decode_plan(batch=16, seed=5)
+@pytest.mark.parametrize("shape", ["gqa", "mqa"])
+def test_merge_in_cuda_graph_replays(cuda_device, shape):
+    plan = wl.gqa_decode_plan(batch=16, seed=5) if shape == "gqa" else _mqa_plan(5)
     st, kp, vp = _appended(plan, cuda_device)
     ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
     q = st.q.clone()
@@ -161,28 +183,32 @@ from serving_slot_mapping_gb300 import capi
 from serving_slot_mapping_gb300 import workloads as wl
 from _parity import assert_close, bits, to_f64
 dev = torch.device("cuda:0")
-plan = wl.gqa_decode_plan(batch=16, seed=6)
-st = wl.materialize(plan, dev)
-kp, vp = st.key_pool.clone(), st.value_pool.clone()
-capi.paged_kv_append(kp, vp, st.key, st.value, st.slot_mapping)  # eager: creates the device error word
-torch.cuda.synchronize()
-ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
-out = torch.full_like(st.q, float("nan"))
-s = torch.cuda.Stream()
-g = torch.cuda.CUDAGraph()
-with torch.cuda.graph(g, stream=s):  # the process's first decode launch: inside a capture
-    capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
-                                max_seq_len=int(plan.seq_lens.max()), out=out, workspace=ws, stream=s)
-for rep in range(2):
-    st.q.copy_(torch.randn(st.q.shape, generator=torch.Generator().manual_seed(rep)).to(st.q.dtype))
-    out.fill_(float("nan"))
+import numpy as np
+plans = [wl.gqa_decode_plan(batch=16, seed=6),
+         wl.plan_from_lengths("mqa_fallback", "decode", "bf16", 32, 1, 128, 16,
+                              np.full(32, 3000) + np.arange(32) * 7, np.ones(32), seed=6)]
+for i, plan in enumerate(plans):
+    st = wl.materialize(plan, dev)
+    kp, vp = st.key_pool.clone(), st.value_pool.clone()
+    capi.paged_kv_append(kp, vp, st.key, st.value, st.slot_mapping)  # eager: creates the device error word
     torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    assert capi.device_error() == (0, 0)
-    exp = oracle.paged_attention_decode(to_f64(bits(kp)), to_f64(bits(vp)), to_f64(bits(st.q)),
-                                        plan.block_table, plan.seq_lens, plan.scale)
-    assert_close(out, exp, "bf16", f"whole-segment merge, replay {rep}")
+    ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
+    out = torch.full_like(st.q, float("nan"))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):  # the process's first decode launch: inside a capture
+        capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                    max_seq_len=int(plan.seq_lens.max()), out=out, workspace=ws, stream=s)
+    for rep in range(2):
+        st.q.copy_(torch.randn(st.q.shape, generator=torch.Generator().manual_seed(rep)).to(st.q.dtype))
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert capi.device_error() == (0, 0)
+        exp = oracle.paged_attention_decode(to_f64(bits(kp)), to_f64(bits(vp)), to_f64(bits(st.q)),
+                                            plan.block_table, plan.seq_lens, plan.scale)
+        assert_close(out, exp, "bf16", f"whole-segment merge, plan {i}, replay {rep}")
 print("fallback merge ok")
 """
 
@@ -202,7 +228,8 @@ def test_merge_without_cooperative_launch():
     assert "fallback merge ok" in out.stdout
 
 
-def test_bounded_part_wait_runs_out_and_is_reported(cuda_device):
+@pytest.mark.parametrize("shape", ["gqa", "mqa"])
+def test_bounded_part_wait_runs_out_and_is_reported(cuda_device, shape):
     """The decode kernel's one wait on other CTAs (a CTA holding part of a cut
     segment waits for the other parts before merging its slice) is bounded.
     Through the test hook every cut segment expects one part that never
@@ -210,7 +237,8 @@ def test_bounded_part_wait_runs_out_and_is_reported(cuda_device):
     instead of hanging, record code 5 (a bounded wait gave up, detail -2 =
     the part wait) in the device error word, and leave the context usable --
     a normal decode on the same workspace afterwards matches the oracle."""
-    plan = wl.gqa_decode_plan(batch=32, seed=23)      # ~145 blocks a sequence over 152 CTAs: all cut
+    # ~145 (GQA) or ~190 (MQA) blocks a sequence over 152 CTAs: every segment is cut
+    plan = wl.gqa_decode_plan(batch=32, seed=23) if shape == "gqa" else _mqa_plan(23)
     st, kp, vp = _appended(plan, cuda_device)
     ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
     capi.device_error()

@@ -148,7 +148,7 @@ def test_long_context_full_every_sequence(cuda_device, hkv):
 # ragged, edge and degenerate cases
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (32, 8), (16, 1), (32, 1), (6, 3)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (32, 8), (16, 1), (32, 1), (6, 3), (64, 2), (128, 4)])
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_groups_and_head_dims(cuda_device, hq, hkv, d):
     lens = [1, 15, 16, 17, 31, 33, 100, 257, 1000]
