@@ -16,6 +16,9 @@
 //   page_size 8).  All units are laid out sequence-major and cut into
 //   `num_ctas` equal contiguous ranges, one persistent CTA per SM, so every
 //   CTA streams the same number of KV bytes whatever the context-length mix.
+//   For 32-row groups, where a segment change costs a CTA ~5 us, each segment
+//   also weighs seg_penalty blocks in the cut, and a publisher warp counts the
+//   CTA's cut segments off the consumer path.
 // * Two producer warps (even and odd stages) follow block_table and load each
 //   stage (NBS blocks x HB heads of K and V) with TMA tensor copies through a
 //   4-D view of the pool {64 dims, slots, kv_heads, slabs}: one box
