@@ -157,6 +157,16 @@ def test_decode_groups_and_head_dims(cuda_device, hq, hkv, d):
     _check_step(plan, cuda_device, plan.name)
 
 
+def test_decode_32_row_groups_weighted_cut(cuda_device):
+    """32 query heads per KV head with 4 KV heads (one box of 4): enough
+    blocks per CTA that segment changes weigh in the cut of the units (the
+    plain cut is used for the smaller shapes above)."""
+    lens = np.full(32, 1000) + np.arange(32) * 37
+    plan = wl.plan_from_lengths("dec_128_4_weighted", "decode", "bf16", 128, 4, 128, 16,
+                                lens - 1, np.ones(32), seed=4141)
+    _check_step(plan, cuda_device, plan.name)
+
+
 @pytest.mark.parametrize("ps", [8, 32, 64, 256])
 def test_decode_page_sizes(cuda_device, ps):
     lens = [3, 64, 65, 190, 511]
