@@ -64,6 +64,25 @@ def test_decode_csr_ragged(cuda_device, hq, hkv, d, ps):
     assert_close(out, exp, plan.dtype, "decode csr ragged")
 
 
+def test_decode_csr_32_row_groups(cuda_device):
+    # 32 query heads on 1 KV head, ~190 blocks a sequence: the weighted cut
+    lens = np.full(32, 3000) + np.arange(32) * 7
+    plan = wl.plan_from_lengths("csr_mqa_weighted", "decode", "bf16", 32, 1, 128, 16, lens - 1,
+                                np.ones(32), seed=48, extra_free_pages=5)
+    st = wl.materialize(plan, cuda_device)
+    kp, vp, dense = gpu_step(st)
+    (ip, ix, last), host = _csr_dev(plan, cuda_device)
+    out = capi.paged_attention_decode_csr(kp, vp, st.q, ip, ix, last, plan.scale,
+                                          max_seq_len=int(lens.max()))
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    assert torch.equal(out.view(torch.int16), dense.view(torch.int16))
+    K, V = _oracle_pools(st)
+    seqs = list(range(0, plan.batch, 4))
+    exp = oracle.paged_attention_decode_csr(K, V, to_f64(bits(st.q)), *host, plan.scale, seqs=seqs)
+    assert_close(out, exp, plan.dtype, "decode csr 32-row groups", rows=seqs)
+
+
 @pytest.mark.parametrize("ps", [8, 16, 256])
 def test_prefill_csr(cuda_device, ps):
     plan = wl.chunked_prefill_plan(new=(64, 100, 1, 17, 250), cached=(0, 300, 47, 0, 33), seed=ps, ps=ps)

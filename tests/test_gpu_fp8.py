@@ -71,6 +71,20 @@ def test_fp8_decode_ragged(cuda_device, hq, hkv, d, ps):
     assert_close(out, exp, "bf16", f"fp8 decode {hq}/{hkv}/{d} ps{ps}")
 
 
+def test_fp8_decode_32_row_groups_weighted_cut(cuda_device):
+    lens = np.full(32, 3000) + np.arange(32) * 7   # ~190 blocks a sequence on 1 KV head
+    plan = wl.plan_from_lengths("fp8_mqa_weighted", "decode", "bf16", 32, 1, 128, 16, lens - 1,
+                                np.ones(32), seed=49, extra_free_pages=4)
+    kp, vp, kc, vc, st = _fp8_step(plan, cuda_device, ks=0.02, vs=0.03)
+    out = capi.paged_attention_decode(kp, vp, st.q, st.block_table, st.seq_lens, plan.scale,
+                                      max_seq_len=int(lens.max()), k_scale=0.02, v_scale=0.03)
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    exp = kv_fp8.paged_attention_decode_fp8(kc, vc, 0.02, 0.03, to_f64(bits(st.q)), plan.block_table,
+                                            plan.seq_lens, plan.scale)
+    assert_close(out, exp, "bf16", "fp8 decode 32-row groups")
+
+
 def test_fp8_decode_csr_and_static_scratch_match(cuda_device):
     plan = wl.gqa_decode_plan(batch=9, lo=100, hi=2000, seed=21)
     kp, vp, kc, vc, st = _fp8_step(plan, cuda_device)

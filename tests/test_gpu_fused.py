@@ -78,6 +78,15 @@ def test_fused_ragged(cuda_device, hq, hkv, d, ps):
     _check(plan, cuda_device, plan.name)
 
 
+def test_fused_32_row_groups(cuda_device):
+    # 32 query heads on 1 KV head, ~190 blocks a sequence: segment changes weigh
+    # in the cut and a publisher warp counts the cut segments
+    lens = np.full(32, 3000) + np.arange(32) * 7
+    plan = wl.plan_from_lengths("fused_mqa_weighted", "decode", "bf16", 32, 1, 128, 16, lens - 1,
+                                np.ones(32), seed=47, extra_free_pages=4)
+    _check(plan, cuda_device, plan.name)
+
+
 def test_fused_long_context(cuda_device):
     _check(wl.long_context_plan(hkv=8, batch=12, lo=1000, hi=9000, seed=41), cuda_device, "fused long")
 
