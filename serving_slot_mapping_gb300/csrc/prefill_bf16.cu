@@ -113,7 +113,14 @@ __device__ __forceinline__ void convert_tile_e4m3(unsigned char* slot, int valid
   constexpr int kLoads = 8 / kKeysPerLoad;    // loads per lane per 8-key block (2 or 1)
   constexpr int kRowBlock = (D / 64) * 1024;  // bytes of one 8-key block in f16
   const unsigned char* codes = slot + kBN * D;
-  const int m = lane % kChunks, r0 = lane / kChunks;
+  // lane -> (key r0 of the load's keys, 16-code chunk m).  D = 128: each
+  // quarter-warp takes chunks 0..3 of one key and 4..7 of the key beside it
+  // (key rows 8 apart in r0 & 1), so a quarter's 16-byte loads hit 8 bank
+  // groups and so do its f16 stores (even and odd chunks XOR key % 8 of two
+  // keys of different parity); D = 64: chunk lane % 4 of key lane / 4 does both.
+  const int q4 = lane >> 3, j8 = lane & 7;
+  const int m = D == 128 ? (j8 & 3) + 4 * (j8 >> 2) : lane % kChunks;
+  const int r0 = D == 128 ? 2 * (q4 >> 1) + ((j8 >> 2) ^ (q4 & 1)) : lane / kChunks;
 #pragma unroll 1
   for (int k0 = 0; k0 < kBN / 8; k0 += 4) {
     uint4 raw[4][kLoads];
