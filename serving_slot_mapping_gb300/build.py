@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_fused.cu", "prefill_bf16.cu", "attn_f32.cu",
+SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_fused.cu", "decode_weighted.cu", "prefill_bf16.cu", "attn_f32.cu",
            "decode_noalloc.cu", "tmap.cu"]
 HEADERS = ["common.cuh", "internal.h", "tma.cuh", "tcgen05.cuh", "decode_split.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

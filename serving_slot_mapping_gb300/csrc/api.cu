@@ -273,8 +273,9 @@ pa_status bf16_decode_params(const pa_kv_pool* pool, const void* q, void* out, i
   p->kv8 = kv8(pool) ? 1 : 0;
   p->scale_log2 = (float)((double)scale * (kv8(pool) ? (double)pool->k_scale : 1.0) * kLog2e);
   p->v_scale = kv8(pool) ? pool->v_scale : 1.f;
-  // segment changes weigh in the cut (32-row groups); positions are counted in 32 bits
-  const int pen = pa::decode_segment_penalty(pool->head_dim, hb, group, kv8(pool));
+  // segment changes weigh in the cut (32-row groups; 16-row groups of few long
+  // sequences); positions are counted in 32 bits
+  const int pen = pa::decode_segment_penalty(pool->head_dim, hb, group, kv8(pool), batch, pool->num_kv_heads, ctas);
   const int64_t max_keys = std::max<int64_t>(max_seq_len, (int64_t)t.max_blocks * pool->page_size);
   p->seg_penalty = (int64_t)batch * ((max_keys + 15) / 16 + pen) <= INT32_MAX ? pen : 0;
   p->err = error_word();

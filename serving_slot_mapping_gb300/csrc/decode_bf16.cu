@@ -146,9 +146,21 @@ int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size)
 // segment's query rows).  In 16-key blocks of one head box that is the
 // change's time over one block's: its K and V bytes at ~46 GB/s (an SM's share
 // of HBM) or its MMA work at ~0.35 ns per query-key pair, whichever is longer.
-// Other shapes cut the units plainly (0).
-int decode_segment_penalty(int32_t head_dim, int32_t heads_per_box, int32_t group, bool kv8) {
-  if (group <= 16) return 0;
+// 16-row groups in boxes of 8 heads of 128 dims whose segments (sequence x
+// head box) number at most a quarter of the CTAs, so that each is cut across
+// four or more CTA ranges on average: the WC instantiations, 8 blocks (bf16)
+// or 12 (e4m3).  There the CTAs whose ranges hold two cut segments (two
+// counts, two merges) finish last; per-CTA stamps put them ~2.6 us per extra
+// segment behind.  The weights were set by measurement on GB300 (batch 32 of
+// 512-4096 keys, 32/8 heads, weights 4 to 12 tried: bf16 63.2 -> 60.7 us at
+// 8, e4m3 47.6 -> 45.0 us at 12).  Other shapes cut the units plainly (0).
+int decode_segment_penalty(int32_t head_dim, int32_t heads_per_box, int32_t group, bool kv8, int32_t batch,
+                           int32_t num_kv_heads, int32_t num_ctas) {
+  if (group <= 16) {
+    if (head_dim != 128 || heads_per_box != 8) return 0;
+    const int64_t segments = (int64_t)batch * (num_kv_heads / heads_per_box);
+    return 4 * segments <= num_ctas ? (kv8 ? 12 : 8) : 0;
+  }
   const double bytes_ns = 2.0 * 16 * heads_per_box * head_dim * (kv8 ? 1 : 2) / 46.0;
   const double mma_ns = 16.0 * heads_per_box * group * 0.35;
   return (int)(5000.0 / (bytes_ns > mma_ns ? bytes_ns : mma_ns) + 0.5);

@@ -1,9 +1,10 @@
 // The split-KV decode kernel of paged_attention_decode (bf16 and e4m3 pools),
 // templated on the shape (head_dim, heads per box, row tiles), the pool
 // element type and FUSED (paged_attention_decode_append: the kernel also
-// writes the step's new K/V rows and attends to them from its input).  The
-// plain instantiations are compiled in decode_bf16.cu, the fused ones in
-// decode_fused.cu, so a plain decode carries none of the fused code.
+// writes the step's new K/V rows and attends to them from its input) and WC
+// (the weighted cut below for 16-row groups).  The plain instantiations are
+// compiled in decode_bf16.cu, the fused ones in decode_fused.cu, the WC ones in
+// decode_weighted.cu, so a plain decode carries none of the fused code.
 //
 // What is computed (onnxruntime/mobius PR #395 "Add paged / block-table KV
 // cache export", "How it works": Gather(pool, block_table) then Attention
@@ -18,7 +19,8 @@
 //   CTA streams the same number of KV bytes whatever the context-length mix.
 //   For 32-row groups, where a segment change costs a CTA ~5 us, each segment
 //   also weighs seg_penalty blocks in the cut, and a publisher warp counts the
-//   CTA's cut segments off the consumer path.
+//   CTA's cut segments off the consumer path; the WC instantiations do the same
+//   for 16-row groups of long sequences (each cut across several CTAs).
 // * Two producer warps (even and odd stages) follow block_table and load each
 //   stage (NBS blocks x HB heads of K and V) with TMA tensor copies through a
 //   4-D view of the pool {64 dims, slots, kv_heads, slabs}: one box
@@ -264,8 +266,9 @@ __device__ __noinline__ void merge_segment(const DecodeParams& p, int b, int hkb
   }
 }
 
-// Compile-time shape of one configuration: HB heads per box, RT row tiles.
-template <int D, int HB, int RT, bool KV8 = false>
+// Compile-time shape of one configuration: HB heads per box, RT row tiles,
+// WC the weighted cut and publisher warp for 16-row groups.
+template <int D, int HB, int RT, bool KV8 = false, bool WC = false>
 struct Cfg {
   static constexpr int kConsumers = 8;
   // 16-key blocks a consumer warp takes per stage: two for 32-row groups, so
@@ -278,8 +281,10 @@ struct Cfg {
   // 32-row groups: a segment change costs a CTA ~5 us (the NW warps' chained
   // merge, the part's write and count), so the cut of the units weighs
   // segment changes (seg_penalty) and a publisher warp does each cut
-  // segment's fence and count off the consumer path
-  static constexpr bool kCostlyChange = RT == 2;
+  // segment's fence and count off the consumer path; with WC, 16-row groups
+  // whose sequences each span several CTAs too (the CTAs holding two cut
+  // segments, two counts and two merges, set the call's time)
+  static constexpr bool kCostlyChange = RT == 2 || WC;
   // + the Q producer warp (+ the publisher warp)
   static constexpr int kThreads = 32 * (kConsumers + kKvProducers + 1 + (kCostlyChange ? 1 : 0));
   static constexpr int kBars = kCostlyChange ? 7 : 4;  // mbarriers after the ring's two per stage
@@ -311,9 +316,9 @@ struct Layout {
   int stages, qslot, bar_off, mrg_off, prefix_off, total;
 };
 
-template <int D, int HB, int RT, bool KV8 = false>
+template <int D, int HB, int RT, bool KV8 = false, bool WC = false>
 __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
-  using C = Cfg<D, HB, RT, KV8>;
+  using C = Cfg<D, HB, RT, KV8, WC>;
   Layout L;
   L.qslot = ((HB * G * D * 2) + 127) / 128 * 128;
   const int merge = C::NW > 1 ? HB * G * (D + 2) * 4 : 0;  // one slot: the chained merge below
@@ -329,11 +334,11 @@ __host__ __device__ inline Layout make_layout(int G, int B, int budget) {
   return L;
 }
 
-template <int D, int HB, int RT, bool KV8, bool FUSED>
-__global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
+template <int D, int HB, int RT, bool KV8, bool FUSED, bool WC = false>
+__global__ void __launch_bounds__(Cfg<D, HB, RT, KV8, WC>::kThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         DecodeParams p) {
-  using C = Cfg<D, HB, RT, KV8>;
+  using C = Cfg<D, HB, RT, KV8, WC>;
   constexpr int NBS = C::NBS, BPW = C::BPW, NW = C::NW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
   const int Hkv = p.pool.num_kv_heads;
   const int Hg = Hkv / HB;  // head boxes per sequence
   const int Hq = p.num_q_heads;
-  const Layout lay = make_layout<D, HB, RT, KV8>(G, B, p.smem_budget);
+  const Layout lay = make_layout<D, HB, RT, KV8, WC>(G, B, p.smem_budget);
   const int S = lay.stages;
   unsigned char* ring = smem;
   unsigned char* qring = smem + S * C::kStageBytes;
@@ -1204,14 +1209,19 @@ __global__ void __launch_bounds__(Cfg<D, HB, RT, KV8>::kThreads, 1)
 int coop_launch_state();
 void set_coop_launch_state(int v);
 
+// head_dim 128, 8 heads per box, 16-row groups, seg_penalty > 0: the WC
+// instantiations (decode_weighted.cu)
+cudaError_t launch_split_weighted(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, bool kv8,
+                                  bool fused, cudaStream_t s);
+
 namespace {
 
-template <int D, int HB, int RT, bool KV8, bool FUSED>
+template <int D, int HB, int RT, bool KV8, bool FUSED, bool WC = false>
 cudaError_t launch_split(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
-  using C = Cfg<D, HB, RT, KV8>;
-  const Layout lay = make_layout<D, HB, RT, KV8>(p.group, p.batch, p.smem_budget);
+  using C = Cfg<D, HB, RT, KV8, WC>;
+  const Layout lay = make_layout<D, HB, RT, KV8, WC>(p.group, p.batch, p.smem_budget);
   if (lay.stages < 2) return cudaErrorInvalidConfiguration;
-  auto kern = decode_split_kernel<D, HB, RT, KV8, FUSED>;
+  auto kern = decode_split_kernel<D, HB, RT, KV8, FUSED, WC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
   // Plain decode: a co-resident (cooperative) grid lets every CTA of a cut
@@ -1242,7 +1252,12 @@ template <int D, bool KV8, bool FUSED>
 cudaError_t launch_split_d(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int rt,
                            cudaStream_t s) {
   switch (p.heads_per_box * 10 + rt) {
-    case 81: return launch_split<D, 8, 1, KV8, FUSED>(p, tk, tv, s);
+    case 81:
+      // 16-row groups in boxes of 8 heads with a segment penalty: the WC
+      // instantiation (decode_weighted.cu)
+      if constexpr (D == 128)
+        if (p.seg_penalty > 0) return launch_split_weighted(p, tk, tv, KV8, FUSED, s);
+      return launch_split<D, 8, 1, KV8, FUSED>(p, tk, tv, s);
     case 41: return launch_split<D, 4, 1, KV8, FUSED>(p, tk, tv, s);
     case 21: return launch_split<D, 2, 1, KV8, FUSED>(p, tk, tv, s);
     case 11: return launch_split<D, 1, 1, KV8, FUSED>(p, tk, tv, s);

@@ -96,15 +96,17 @@ struct DecodeParams {
   const float* pre_o;     // [pre_chunks, B, Hq, D] fp32 unnormalised
   const float2* pre_ml;   // [pre_chunks, B, Hq] (reference max in log2 units, denominator)
   int32_t pre_chunks;
-  // 32-row groups: the weight of a segment (sequence x head box) in the cut
-  // of the units into CTA ranges, in 16-key blocks of the box (the time a CTA
-  // loses at a segment change over one block's time; decode_segment_penalty).
-  // 0 for cascade decode, whose combine kernel recomputes the plain cut.
+  // 32-row groups, and 16-row groups of few long sequences (the WC
+  // instantiations, chosen when this is > 0): the weight of a segment
+  // (sequence x head box) in the cut of the units into CTA ranges, in 16-key
+  // blocks of the box (decode_segment_penalty).  0 for cascade decode, whose
+  // combine kernel recomputes the plain cut.
   int32_t seg_penalty;
 };
 // Number of partial slots the split kernel may write for this launch.
 int decode_heads_per_box(int32_t num_kv_heads, int32_t group, int32_t page_size);
-int decode_segment_penalty(int32_t head_dim, int32_t heads_per_box, int32_t group, bool kv8);
+int decode_segment_penalty(int32_t head_dim, int32_t heads_per_box, int32_t group, bool kv8, int32_t batch,
+                           int32_t num_kv_heads, int32_t num_ctas);
 int64_t decode_partial_slots(int32_t batch, int32_t num_kv_heads, int32_t num_ctas, int32_t heads_per_box);
 int decode_num_ctas(int num_sms, int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t heads_per_box);
 // Launch the fused (append + decode) split kernel (decode_fused.cu).

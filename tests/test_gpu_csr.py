@@ -83,6 +83,25 @@ def test_decode_csr_32_row_groups(cuda_device):
     assert_close(out, exp, plan.dtype, "decode csr 32-row groups", rows=seqs)
 
 
+def test_decode_csr_16_row_groups_weighted(cuda_device):
+    # 32/8 heads, 20 sequences of 800-4000 keys: each spans several CTA
+    # ranges, so segment changes weigh in the cut (the weighted instantiation)
+    lens = np.random.RandomState(49).randint(800, 4000, size=20)
+    plan = wl.plan_from_lengths("csr_gqa_weighted", "decode", "bf16", 32, 8, 128, 16, lens - 1,
+                                np.ones(20), seed=49, extra_free_pages=5)
+    st = wl.materialize(plan, cuda_device)
+    kp, vp, dense = gpu_step(st)
+    (ip, ix, last), host = _csr_dev(plan, cuda_device)
+    out = capi.paged_attention_decode_csr(kp, vp, st.q, ip, ix, last, plan.scale,
+                                          max_seq_len=int(lens.max()))
+    torch.cuda.synchronize()
+    assert capi.device_error() == (0, 0)
+    assert torch.equal(out.view(torch.int16), dense.view(torch.int16))
+    K, V = _oracle_pools(st)
+    exp = oracle.paged_attention_decode_csr(K, V, to_f64(bits(st.q)), *host, plan.scale)
+    assert_close(out, exp, plan.dtype, "decode csr 16-row groups, weighted cut")
+
+
 @pytest.mark.parametrize("ps", [8, 16, 256])
 def test_prefill_csr(cuda_device, ps):
     plan = wl.chunked_prefill_plan(new=(64, 100, 1, 17, 250), cached=(0, 300, 47, 0, 33), seed=ps, ps=ps)

@@ -125,9 +125,20 @@ def test_merge_repeated_calls_and_shapes_share_one_workspace(cuda_device):
             assert_close(out, _expect(st, kp, vp, q), "bf16", f"merge rep {rep} plan {i}")
 
 
-@pytest.mark.parametrize("shape", ["gqa", "mqa"])
+def _plan_of(shape, seed):
+    # gqa: 16 or 32 long sequences, few enough that segment changes weigh in
+    # the cut (the weighted instantiation); gqa_plain_cut: 64, cut plainly;
+    # mqa: 32-row groups
+    if shape == "gqa":
+        return wl.gqa_decode_plan(batch=16 if seed == 5 else 32, seed=seed)
+    if shape == "gqa_plain_cut":
+        return wl.gqa_decode_plan(batch=64, seed=seed)
+    return _mqa_plan(seed)
+
+
+@pytest.mark.parametrize("shape", ["gqa", "gqa_plain_cut", "mqa"])
 def test_merge_in_cuda_graph_replays(cuda_device, shape):
-    plan = wl.gqa_decode_plan(batch=16, seed=5) if shape == "gqa" else _mqa_plan(5)
+    plan = _plan_of(shape, 5)
     st, kp, vp = _appended(plan, cuda_device)
     ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
     q = st.q.clone()
@@ -184,7 +195,7 @@ from serving_slot_mapping_gb300 import workloads as wl
 from _parity import assert_close, bits, to_f64
 dev = torch.device("cuda:0")
 import numpy as np
-plans = [wl.gqa_decode_plan(batch=16, seed=6),
+plans = [wl.gqa_decode_plan(batch=16, seed=6), wl.gqa_decode_plan(batch=64, seed=6),
          wl.plan_from_lengths("mqa_fallback", "decode", "bf16", 32, 1, 128, 16,
                               np.full(32, 3000) + np.arange(32) * 7, np.ones(32), seed=6)]
 for i, plan in enumerate(plans):
@@ -228,7 +239,7 @@ def test_merge_without_cooperative_launch():
     assert "fallback merge ok" in out.stdout
 
 
-@pytest.mark.parametrize("shape", ["gqa", "mqa"])
+@pytest.mark.parametrize("shape", ["gqa", "gqa_plain_cut", "mqa"])
 def test_bounded_part_wait_runs_out_and_is_reported(cuda_device, shape):
     """The decode kernel's one wait on other CTAs (a CTA holding part of a cut
     segment waits for the other parts before merging its slice) is bounded.
@@ -238,7 +249,7 @@ def test_bounded_part_wait_runs_out_and_is_reported(cuda_device, shape):
     the part wait) in the device error word, and leave the context usable --
     a normal decode on the same workspace afterwards matches the oracle."""
     # ~145 (GQA) or ~190 (MQA) blocks a sequence over 152 CTAs: every segment is cut
-    plan = wl.gqa_decode_plan(batch=32, seed=23) if shape == "gqa" else _mqa_plan(23)
+    plan = _plan_of(shape, 23)
     st, kp, vp = _appended(plan, cuda_device)
     ws = capi.decode_workspace(plan.batch, plan.num_q_heads, kp)
     capi.device_error()

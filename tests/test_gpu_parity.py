@@ -167,6 +167,24 @@ def test_decode_32_row_groups_weighted_cut(cuda_device):
     _check_step(plan, cuda_device, plan.name)
 
 
+def test_decode_16_row_groups_weighted_cut(cuda_device):
+    """32/8 heads, d 128, 24 sequences (few enough that each spans several
+    CTA ranges: segment changes weigh in the cut and a publisher warp counts
+    the parts), with empty, one-key and one-page sequences between long ones."""
+    rng = np.random.RandomState(77)
+    lens = rng.randint(600, 5000, size=24)
+    lens[[3, 11, 20]] = 0
+    lens[[5, 17]] = 1
+    lens[8] = 16
+    plan = wl.plan_from_lengths("dec_16_rows_weighted", "decode", "bf16", 32, 8, 128, 16,
+                                np.maximum(lens - 1, 0), (lens > 0).astype(int), seed=4242)
+    st = wl.materialize(plan, cuda_device)
+    kp, vp, out = gpu_step(st)
+    kb, vb, exp = oracle_step(st)
+    assert_close(out, exp, "bf16", plan.name)
+    assert torch.all(out[3] == 0) and torch.all(out[11] == 0) and torch.all(out[20] == 0)
+
+
 @pytest.mark.parametrize("ps", [8, 32, 64, 256])
 def test_decode_page_sizes(cuda_device, ps):
     lens = [3, 64, 65, 190, 511]
