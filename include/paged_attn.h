@@ -16,8 +16,12 @@
  * --------------------------------
  * - All tensor arguments are DEVICE pointers on the current CUDA device,
  *   owned by the caller.  The library allocates no device memory and keeps
- *   no per-call state; the only library state is one device-side error
- *   word per device (see paged_device_error).
+ *   no per-call state.  Its state: one device-side error word per device
+ *   (see paged_device_error); a process-wide note of whether the runtime
+ *   accepts the decode kernel's cooperative launch (learnt on the first eager
+ *   decode launch); and, for paged_attention_decode_cascade only, one extra
+ *   stream and two events per (host thread, device), created by the first
+ *   cascade call on that thread and kept for the thread's life.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *   default stream).  Host-side argument checks run before any launch; on a
  *   non-PA_OK return nothing was launched.
@@ -217,7 +221,10 @@ pa_status paged_attention_prefill_csr(const pa_kv_pool* pool, const void* q, voi
  * prefix is read once for all B query rows (one tensor-core pass with its keys
  * cut into chunks, fp32 partials) instead of once per sequence; each sequence's
  * own tokens go through the split-KV decode, and the partials of both are
- * merged per row.
+ * merged per row.  The prefix pass runs on a second stream of the library's,
+ * forked from `stream` and joined back to it with events (so stream order and
+ * stream capture hold); that stream is created by the first cascade call on a
+ * host thread, which must therefore come before any stream capture there.
  *
  * prefix_block_ids  device int32 [ceil(prefix_len / page_size)], the shared
  *                   pages in order (the prefix may end inside its last page).
