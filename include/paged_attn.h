@@ -148,14 +148,16 @@ pa_status paged_kv_append(const pa_kv_pool* pool, const void* key, const void* v
  * of a cut segment each merge a slice of it), so its start can wait for SMs
  * held by kernels on other streams.  Where the runtime refuses that launch,
  * the CTA that counts a segment's last part merges the whole segment.
- * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most 32
- * query heads per KV head, q 16-byte aligned, at most 2^31 - 1 slots
- * (num_pages * page_size) per pool and batch * ceil(max_seq_len / 16) below
- * 2^31 (PA_ERR_RANGE beyond);
+ * bf16 path (tensor cores): page_size a power of two >= 8, head_dim in
+ * {64, 128}, at most 32 query heads per KV head, q 16-byte aligned, at most
+ * 2^31 - 1 slots (num_pages * page_size) per pool and batch *
+ * ceil(max_seq_len / 16) below 2^31 (PA_ERR_RANGE beyond);
  * e4m3 pools: the bf16 limits; q and out are bf16; the attention is that of
  * the values the codes stand for (scale * k_scale * q . e4m3(K), outputs
  * times v_scale), computed with f16 products (every e4m3 value is an f16);
- * f32 path: head_dim <= 256, any page_size.
+ * CUDA-core path (fp32 arithmetic, one key at a time; correct, not fast):
+ * f32 pools, and bf16 pools of any other page_size (1, 2, 4, or not a power
+ * of two); head_dim <= 256, no workspace used.
  */
 size_t paged_attention_decode_workspace_size(int32_t batch, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim,
@@ -237,8 +239,9 @@ pa_status paged_attention_prefill_csr(const pa_kv_pool* pool, const void* q, voi
  * workspace         device scratch of at least
  *                   paged_attention_decode_cascade_workspace_size(...) bytes,
  *                   16-byte aligned; contents need no initialisation.
- * bf16 pools only (PA_ERR_UNSUPPORTED for f32), with the bf16 limits of
- * paged_attention_decode.
+ * bf16 pools only (PA_ERR_UNSUPPORTED for f32), with the tensor-core limits
+ * of paged_attention_decode (a page_size that is not a power of two >= 8
+ * gives PA_ERR_UNSUPPORTED when prefix_len > 0).
  */
 size_t paged_attention_decode_cascade_workspace_size(int32_t batch, int32_t num_q_heads,
                                                      int32_t num_kv_heads, int32_t head_dim,
@@ -274,8 +277,8 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
  *               (quantised as paged_kv_append does).
  * slot_mapping  device int64 [batch], 8-byte aligned.
  * Every other argument, limit and the workspace are those of
- * paged_attention_decode.  f32 pools run the append and the decode as two
- * launches.
+ * paged_attention_decode.  The CUDA-core path (f32 pools, bf16 pools of
+ * other page sizes) runs the append and the decode as two launches.
  */
 pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key, const void* value,
                                         const int64_t* slot_mapping, const void* q, void* out,
@@ -338,14 +341,15 @@ pa_status paged_attention_decode_static_scratch(const pa_kv_pool* pool, const vo
  *                  [batch] = total_q.
  * max_q_len        host upper bound of n_b (sizes the launch).
  * block_table, seq_lens, max_seq_len, scale: as for decode.
- * bf16 path: head_dim in {64, 128}, page_size a power of two >= 8, at most
- * 32 query heads per KV head;
+ * bf16 path (tensor cores): page_size a power of two >= 8, head_dim in
+ * {64, 128}, at most 32 query heads per KV head;
  * e4m3 pools: the bf16 limits, q 16-byte aligned; q and out are bf16; the
  * attention is that of the values the codes stand for (scale * k_scale *
  * q . e4m3(K), outputs times v_scale), computed with f16 products: q is
  * rounded to f16 (exact for bf16 values of magnitude 2^-14 .. 65504), the
  * codes are exact in f16, and the softmax weights are rounded to f16;
- * f32 path: head_dim <= 256, any page_size.
+ * CUDA-core path (fp32 arithmetic): f32 pools, and bf16 pools of any other
+ * page_size; head_dim <= 256.
  */
 pa_status paged_attention_prefill(const pa_kv_pool* pool, const void* q, void* out,
                                   int32_t batch, int32_t num_q_heads,

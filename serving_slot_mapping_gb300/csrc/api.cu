@@ -62,6 +62,15 @@ size_t elem_size(int32_t dtype) { return dtype == PA_DTYPE_F32 ? 4 : (dtype == P
 
 bool kv8(const pa_kv_pool* pool) { return pool->dtype == PA_DTYPE_FP8_E4M3; }
 
+// Pages the TMA boxes of the tensor-core kernels take: whole 8-slot blocks.
+bool tma_pages(const pa_kv_pool* pool) { return is_pow2(pool->page_size) && pool->page_size >= 8; }
+
+// The CUDA-core attention path (attn_f32.cu): f32 pools, and bf16 pools of
+// other page sizes (1, 2, 4, or not a power of two).
+bool core_path(const pa_kv_pool* pool) {
+  return pool->dtype == PA_DTYPE_F32 || (pool->dtype == PA_DTYPE_BF16 && !tma_pages(pool));
+}
+
 pa_status check_pool(const pa_kv_pool* pool) {
   if (pool == nullptr || pool->key_pool == nullptr || pool->value_pool == nullptr) return PA_ERR_NULL;
   if (pool->dtype != PA_DTYPE_F32 && pool->dtype != PA_DTYPE_BF16 && pool->dtype != PA_DTYPE_FP8_E4M3)
@@ -99,10 +108,10 @@ pa_status check_attention(const pa_kv_pool* pool, int32_t batch, int32_t num_q_h
   if ((int64_t)max_blocks_per_seq * pool->page_size > INT32_MAX) return PA_ERR_RANGE;
   if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * pool->page_size) return PA_ERR_SHAPE;
   if (!std::isfinite(scale)) return PA_ERR_RANGE;
-  if (pool->dtype != PA_DTYPE_F32) {  // bf16 and e4m3: the TMA / tensor-core paths
+  if (!core_path(pool)) {  // bf16 and e4m3: the TMA / tensor-core paths
     if (pool->head_dim != 64 && pool->head_dim != 128) return PA_ERR_UNSUPPORTED;
-    // page-sized TMA boxes of 8-slot blocks
-    if (!is_pow2(pool->page_size) || pool->page_size < 8) return PA_ERR_UNSUPPORTED;
+    // page-sized TMA boxes of 8-slot blocks (e4m3 pools have no other path)
+    if (!tma_pages(pool)) return PA_ERR_UNSUPPORTED;
     if (num_q_heads / pool->num_kv_heads > 32) return PA_ERR_UNSUPPORTED;
     if (!aligned(pool->key_pool, 16) || !aligned(pool->value_pool, 16)) return PA_ERR_ALIGN;
   } else {
@@ -338,12 +347,13 @@ pa_status decode_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t 
   if (st != PA_OK) return st;
   if (q == out) return PA_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pool->dtype == PA_DTYPE_F32) {
-    if (!aligned(q, 4) || !aligned(out, 4)) return PA_ERR_ALIGN;
+  if (core_path(pool)) {
+    if (!aligned(q, elem_size(pool->dtype)) || !aligned(out, elem_size(pool->dtype))) return PA_ERR_ALIGN;
     pa::AttnF32Params p{};
     p.pool = geom(pool);
-    p.q = static_cast<const float*>(q);
-    p.out = static_cast<float*>(out);
+    p.q = q;
+    p.out = out;
+    p.bf16 = pool->dtype == PA_DTYPE_BF16 ? 1 : 0;
     p.query_start_loc = nullptr;
     p.block_table = t.ids;
     p.seq_lens = t.seq_lens;
@@ -383,11 +393,12 @@ pa_status prefill_impl(const pa_kv_pool* pool, const void* q, void* out, int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const pa::PoolGeom g = geom(pool);
   const int32_t group = num_q_heads / pool->num_kv_heads;
-  if (pool->dtype == PA_DTYPE_F32) {
+  if (core_path(pool)) {
     pa::AttnF32Params p{};
     p.pool = g;
-    p.q = static_cast<const float*>(q);
-    p.out = static_cast<float*>(out);
+    p.q = q;
+    p.out = out;
+    p.bf16 = pool->dtype == PA_DTYPE_BF16 ? 1 : 0;
     p.query_start_loc = query_start_loc;
     p.block_table = t.ids;
     p.seq_lens = t.seq_lens;
@@ -464,6 +475,7 @@ pa_status pa_testing_decode_part_wait(const pa_kv_pool* pool, const void* q, voi
                                       int32_t extra_parts, void* stream) {
   if (pool == nullptr) return PA_ERR_NULL;
   if (pool->dtype != PA_DTYPE_BF16 && pool->dtype != PA_DTYPE_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (!tma_pages(pool)) return PA_ERR_UNSUPPORTED;  // the CUDA-core path has no wait
   // a short limit (1 us .. 2 s) and a bounded count: the hook can only
   // shorten a wait, never lengthen one
   if (wait_ns < 1000u || wait_ns > 2000000000u || extra_parts < 0 || extra_parts > 1024) return PA_ERR_RANGE;
@@ -499,7 +511,7 @@ pa_status paged_attention_decode_append(const pa_kv_pool* pool, const void* key,
   if (st != PA_OK) return st;
   if (q == out) return PA_ERR_SHAPE;
   if (!aligned(slot_mapping, 8)) return PA_ERR_ALIGN;
-  if (pool->dtype == PA_DTYPE_F32) {  // the f32 path: append and decode as two launches
+  if (core_path(pool)) {  // the CUDA-core path: append and decode as two launches
     st = paged_kv_append(pool, key, value, slot_mapping, batch, stream);
     if (st != PA_OK) return st;
     return decode_impl(pool, q, out, batch, num_q_heads, t, max_seq_len, scale, workspace, workspace_bytes, stream);
@@ -549,6 +561,7 @@ pa_status paged_attention_decode_cascade(const pa_kv_pool* pool, const void* q, 
   if (prefix_len == 0)  // nothing shared: plain decode (its workspace is a prefix of this one's)
     return paged_attention_decode(pool, q, out, batch, num_q_heads, block_table, max_blocks_per_seq, seq_lens,
                                   max_seq_len, scale, workspace, workspace_bytes, stream);
+  if (!tma_pages(pool)) return PA_ERR_UNSUPPORTED;  // the prefix pass is the tensor-core kernel
   if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr ||
       prefix_block_ids == nullptr)
     return PA_ERR_NULL;

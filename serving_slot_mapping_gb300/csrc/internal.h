@@ -177,10 +177,13 @@ struct PrefillParams {
 cudaError_t launch_prefill_bf16(const PrefillParams& p, cudaStream_t s);
 
 // ---- fp32 path (decode = prefill with one row per sequence) --------------
+// The CUDA-core path (attn_f32.cu): f32 pools, and bf16 pools whose page
+// size the TMA boxes of the tensor-core kernels cannot take.
 struct AttnF32Params {
   PoolGeom pool;
-  const float* q;         // [rows, Hq, D]
-  float* out;
+  const void* q;          // [rows, Hq, D], the pool's element type
+  void* out;              // [rows, Hq, D], the pool's element type
+  int32_t bf16;           // 1: q, pools and out are bf16 (fp32 arithmetic); 0: f32
   const int32_t* query_start_loc;  // null for decode (row b = sequence b, n_b = 1)
   const int32_t* block_table;      // dense rows, or kv_indices in the CSR form
   const int32_t* seq_lens;         // dense form

@@ -76,8 +76,13 @@ def _decode(L, pool, hq=32, batch=2, mb=4, msl=64, scale=0.1, ws=None, wsb=0, q=
 def test_decode_validation(L):
     assert _decode(L, _pool(), hq=12) == capi.PA_ERR_SHAPE          # 12 % 8 != 0
     assert _decode(L, _pool(d=96)) == capi.PA_ERR_UNSUPPORTED       # bf16 head_dim
-    assert _decode(L, _pool(ps=12), msl=40) == capi.PA_ERR_UNSUPPORTED  # bf16 page_size
-    assert _decode(L, _pool(ps=4), msl=16) == capi.PA_ERR_UNSUPPORTED   # bf16 decode: page_size >= 8
+    # e4m3 pools: page sizes of whole 8-slot blocks only (no CUDA-core path)
+    assert _decode(L, _pool(dtype=capi.PA_DTYPE_FP8_E4M3, ps=12), msl=40) == capi.PA_ERR_UNSUPPORTED
+    assert _decode(L, _pool(dtype=capi.PA_DTYPE_FP8_E4M3, ps=4), msl=16) == capi.PA_ERR_UNSUPPORTED
+    # bf16 pools of other page sizes take the CUDA-core path: its limits
+    assert _decode(L, _pool(ps=4, d=320), msl=16) == capi.PA_ERR_UNSUPPORTED  # head_dim <= 256
+    assert _decode(L, _pool(ps=4), msl=16, q=None) == capi.PA_ERR_NULL
+    assert _decode(L, _pool(ps=4), msl=17) == capi.PA_ERR_SHAPE      # > max_blocks * page_size
     assert _decode(L, _pool(hkv=1), hq=64) == capi.PA_ERR_UNSUPPORTED  # group 64
     assert _decode(L, _pool(), scale=float("nan")) == capi.PA_ERR_RANGE
     assert _decode(L, _pool(), msl=65) == capi.PA_ERR_SHAPE          # > max_blocks * page_size
@@ -103,7 +108,7 @@ def test_prefill_validation(L):
              float("inf"), None) == capi.PA_ERR_RANGE
     assert f(ctypes.byref(p), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 1 << 29, FAKE, 4, FAKE, 64,
              0.1, None) == capi.PA_ERR_RANGE                      # 2^29 tokens x G 4 packed rows
-    p4 = _pool(ps=4)                                                # bf16: page_size >= 8
+    p4 = _pool(dtype=capi.PA_DTYPE_FP8_E4M3, ps=4)                 # e4m3: page_size >= 8
     assert f(ctypes.byref(p4), FAKE, ctypes.c_void_p(0x50000), 2, 32, FAKE, 10, 5, FAKE, 4, FAKE, 16,
              0.1, None) == capi.PA_ERR_UNSUPPORTED
 
@@ -125,6 +130,8 @@ def test_cascade_validation(L):
     assert call(p, args(pre=None)) == capi.PA_ERR_NULL
     assert call(p, args(wsb=16)) == capi.PA_ERR_WORKSPACE
     assert call(p, args(batch=0)) == capi.PA_OK
+    # the prefix pass is the tensor-core kernel: bf16 pages of whole 8-slot blocks
+    assert call(_pool(ps=4), args(msl=16)) == capi.PA_ERR_UNSUPPORTED
     assert L.paged_attention_decode_cascade_workspace_size(4, 32, 8, 128, capi.PA_DTYPE_F32) == 0
 
 
@@ -165,8 +172,8 @@ def test_decode_append_validation(L):
 
 def test_part_wait_hook_validation(L):
     """The wait-expiry test hook can only shorten a wait: limits outside
-    1 us .. 2 s, negative or huge part counts and f32 pools are refused
-    before any launch."""
+    1 us .. 2 s, negative or huge part counts, f32 pools and bf16 pages the
+    tensor-core kernel does not take are refused before any launch."""
     f = L.pa_testing_decode_part_wait
     p = _pool()
 
@@ -178,5 +185,6 @@ def test_part_wait_hook_validation(L):
     assert call(extra=-1) == capi.PA_ERR_RANGE
     assert call(extra=1025) == capi.PA_ERR_RANGE
     assert call(pool=_pool(dtype=capi.PA_DTYPE_F32)) == capi.PA_ERR_UNSUPPORTED
+    assert call(pool=_pool(ps=4)) == capi.PA_ERR_UNSUPPORTED   # the CUDA-core path has no wait
     assert call(ws=None, wsb=0) == capi.PA_ERR_WORKSPACE
     assert f(None, FAKE, FAKE, 2, 32, FAKE, 4, FAKE, 64, 0.1, FAKE, 1, 1_000_000, 1, None) == capi.PA_ERR_NULL
